@@ -1,0 +1,142 @@
+"""Pins for the oracle's whole forward pass.
+
+(1) the grouped (sort-driven) oracle equals the brute-force per-token loop;
+(2) identical experts reduce to one dense MLP scaled by the sum of the top-k
+    weights; (3) E=1, K=1, w=1 equals a textbook dense MLP written with numpy
+    matrix products on weights decoded through the literal e2m1 table;
+(4) results do not depend on tile_m or on which tokens are evaluated;
+(5) dropped (out-of-range) pairs contribute nothing.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_moe_expert_sort_gb300 import inputs
+
+E2M1_TABLE = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def decode_fp4_ref(codes, scales):
+    lo, hi = codes & 15, codes >> 4
+    c = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (codes.shape[-1] * 2,))
+    v = E2M1_TABLE[c & 7] * np.where(c & 8, -1.0, 1.0)
+    return v * np.repeat(np.exp2(scales.astype(np.float64) - 127), 32, axis=-1)
+
+
+def bf16_bits(x):
+    return x.view(torch.int16).numpy().astype(np.uint16)
+
+
+def make_case(T=16, H=256, I=128, E=8, K=2, seed=0, routing="softmax_topk"):
+    x = inputs.make_x(T, H, seed)
+    ids, w = inputs.make_routing(T, E, K, routing, seed)
+    w13 = torch.stack([inputs.expert_w13(e, H, I, seed) for e in range(E)]).numpy()
+    w2 = torch.stack([inputs.expert_w2(e, H, I, seed) for e in range(E)]).numpy()
+    w13q, w13s = oracle.quantize_weights(w13)
+    w2q, w2s = oracle.quantize_weights(w2)
+    return dict(x=bf16_bits(x), xf=x.to(torch.float64).numpy(), ids=ids.numpy(), w=w.numpy(),
+                w13=w13q, w13s=w13s, w2=w2q, w2s=w2s)
+
+
+ACTS = ["silu", "situv2"]
+ADTS = ["bf16", "fp8", "fp4"]
+
+
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("adt", ADTS)
+def test_grouped_equals_dense_loop(act, adt):
+    c = make_case()
+    g64, g16, _, d0 = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                        act, 4.0, 25.0, adt, tile_m=16)
+    d64, d16, d1 = oracle.moe_dense(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                    act, 4.0, 25.0, adt)
+    assert d0 == d1 == 0
+    assert np.max(np.abs(g64 - d64)) <= 1e-12 * max(1.0, np.max(np.abs(d64)))
+    assert np.array_equal(g16, d16)
+
+
+@pytest.mark.parametrize("adt", ADTS)
+def test_identical_experts_reduce_to_one_mlp(adt):
+    c = make_case(T=8, E=6, K=3, routing="uniform", seed=4)
+    E = 6
+    w13 = np.repeat(c["w13"][:1], E, 0)
+    w13s = np.repeat(c["w13s"][:1], E, 0)
+    w2 = np.repeat(c["w2"][:1], E, 0)
+    w2s = np.repeat(c["w2s"][:1], E, 0)
+    out, _, _, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], w13, w13s, w2, w2s, "situv2", 4.0, 25.0, adt)
+    one = np.zeros((8, 1), dtype=np.int32)
+    mlp, _, _, _ = oracle.moe_forward(c["x"], one, np.ones((8, 1), np.float32), w13[:1], w13s[:1], w2[:1],
+                                      w2s[:1], "situv2", 4.0, 25.0, adt)
+    ref = mlp * c["w"].astype(np.float64).sum(axis=1, keepdims=True)
+    assert np.max(np.abs(out - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("act", ACTS)
+def test_single_expert_is_textbook_mlp(act):
+    c = make_case(T=5, E=1, K=1, seed=9)
+    w = np.ones((5, 1), np.float32)
+    ids = np.zeros((5, 1), np.int32)
+    out, out16, inter, _ = oracle.moe_forward(c["x"], ids, w, c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                              act, 4.0, 25.0, "bf16", want_inter=True)
+    W13 = decode_fp4_ref(c["w13"][0], c["w13s"][0])   # [2I, H]
+    W2 = decode_fp4_ref(c["w2"][0], c["w2s"][0])       # [H, I]
+    I = W2.shape[1]
+    gu = c["xf"] @ W13.T
+    g, u = gu[:, :I], gu[:, I:]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    y = g * sig * u if act == "silu" else 4.0 * np.tanh(g / 4.0) * sig * 25.0 * np.tanh(u / 25.0)
+    yq = torch.tensor(y.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(inter, yq)
+    ref = yq @ W2.T
+    assert np.max(np.abs(out - ref)) <= 1e-12 * np.max(np.abs(ref))
+    ref16 = torch.tensor(ref).to(torch.float32).to(torch.bfloat16)  # ref is fp32-exact? check via bits
+    assert np.mean(out16 == bf16_bits(ref16)) > 0.99
+
+
+def test_tile_m_and_subset_invariance():
+    c = make_case(T=24, E=8, K=3, routing="uniform", seed=5)
+    base, b16, binter, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                              "situv2", 4.0, 25.0, "fp8", tile_m=16, want_inter=True)
+    for tm in (1, 8, 128):
+        o, _, _, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                        "situv2", 4.0, 25.0, "fp8", tile_m=tm)
+        assert np.array_equal(o, base)
+    sub = np.array([7, 0, 23, 11], np.int32)
+    o, o16, inter, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                          "situv2", 4.0, 25.0, "fp8", subset=sub, want_inter=True)
+    assert np.array_equal(o, base[sub])
+    assert np.array_equal(o16, b16[sub])
+    K = 3
+    assert np.array_equal(inter, binter.reshape(24, K, -1)[sub].reshape(len(sub) * K, -1))
+
+
+def test_dropped_pairs_contribute_nothing():
+    c = make_case(T=6, E=8, K=2, routing="uniform", seed=6)
+    ids = c["ids"].copy()
+    ids[2, 1] = 8      # out of range
+    ids[4, 0] = -3
+    out, _, _, dropped = oracle.moe_forward(c["x"], ids, c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                            "silu", 4.0, 25.0, "bf16")
+    assert dropped == 2
+    w = c["w"].copy()
+    ids2 = ids.copy()
+    ids2[2, 1] = 0
+    ids2[4, 0] = 0
+    w[2, 1] = 0.0
+    w[4, 0] = 0.0
+    ref, _, _, _ = oracle.moe_forward(c["x"], ids2, w, c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                      "silu", 4.0, 25.0, "bf16")
+    assert np.array_equal(out, ref)
+
+
+def test_a8w4_quantisation_error_band():
+    """Sanity band, not a pin: a8w4 vs the same weights with unquantised
+    activations (the pages see relL2 ~0.057 for their fused a8w4 op)."""
+    c = make_case(T=6, H=3584, I=384, E=4, K=2, routing="uniform", seed=3)
+    a8, _, _, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                     "situv2", 4.0, 25.0, "fp8")
+    a16, _, _, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                      "situv2", 4.0, 25.0, "bf16")
+    rel = np.linalg.norm(a8 - a16) / np.linalg.norm(a16)
+    assert 0.005 < rel < 0.1
