@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the fused two-stage MoE expert computation on GB300.
+
+Workload (default): Kimi-K3 TP8-shard decode, a16w4 -- hidden 3584, inter 384,
+896 experts, top-16 uniform routing, SiTUv2 (beta 4, linear beta 25), bf16
+activations and output, MXFP4 weights ~N(0, 1/sqrt(fan_in)), seed 123.
+A step is one moe_forward (sort -> activation encode -> stage 1 -> stage 2 ->
+combine) over one batch of T tokens; the headline is T = 64 and the line also
+carries the sweep T = 1, 4, 16, 64. Metric: microseconds per call (lower is
+better) and the fraction of the HBM roofline.
+
+--impl reference times the CPU fp64 oracle (the correctness reference) on the
+host cores on a bounded sample of the same workload.
+Replicas only across GPUs: each rank runs its own copy, no collective on the
+data path; the timing is the max over ranks.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from quantized_moe_expert_sort_gb300 import inputs
+
+H, I, E, K = 3584, 384, 896, 16
+SEED = 123
+HEAD_T = 64
+SWEEP_T = [1, 4, 16, 64]
+PAGE_US_A16W4 = {1: 28.3, 4: 42.7, 16: 107.3, 64: 260.6}  # MI355X us1+us2 (aiter PR 4463, Performance)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, v, device):
+    if pg is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception as e:  # no nvidia-smi
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if not (t0 - 0.25 <= ts <= t1 + 0.25):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), smax=float(parts[1]), power=float(parts[2]),
+                                 hw=parts[4], hwt=parts[5], swt=parts[6], pcap=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": self.err or "no nvidia-smi samples in the timed window"}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def device_weights(device, seed=SEED, chunk=32):
+    """MXFP4 weights of all experts, drawn on the device (seeded per expert) and
+    quantised by the library's own GPU quantiser."""
+    import quantized_moe_expert_sort_gb300 as moe
+    w13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
+    w13s = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device=device)
+    w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
+    w2s = torch.empty((E, H, I // 32), dtype=torch.uint8, device=device)
+    for e in range(E):
+        a = inputs.expert_w13(e, H, I, seed, device=device)
+        w13[e], w13s[e] = moe.quantize_mxfp4(a)
+        b = inputs.expert_w2(e, H, I, seed, device=device)
+        w2[e], w2s[e] = moe.quantize_mxfp4(b)
+    torch.cuda.synchronize(device)
+    return w13, w13s, w2, w2s
+
+
+def batch(T, device, seed=SEED):
+    x = inputs.make_x(T, H, seed)
+    ids, w = inputs.make_routing(T, E, K, "uniform", seed)
+    return x, ids, w, x.to(device), ids.to(device), w.to(device)
+
+
+def algo_bytes(T, n_active, n_pairs, a_bytes=2):
+    """Algorithmic bytes: active experts' weights (fp4 + e8m0), x once, the
+    intermediate written and read once, out once (bf16)."""
+    w13 = n_active * 2 * I * (H // 2 + H // 32)
+    w2 = n_active * H * (I // 2 + I // 32)
+    x = T * H * 2
+    inter = n_pairs * I * a_bytes
+    out = T * H * 2
+    return dict(stage1=w13 + x + inter, stage2=w2 + inter + out, call=w13 + w2 + x + 2 * inter + out)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def stored_traffic(kernel_name, T):
+    """DRAM bytes per launch from a committed ncu summary, if it is current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get("%s_T%d" % (kernel_name, T))
+        if not ent:
+            return None
+        import hashlib
+        src = os.path.join(ROOT, "quantized_moe_expert_sort_gb300", "csrc", ent["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["dram_bytes"] if h == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local, pg):
+    import quantized_moe_expert_sort_gb300 as moe
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    t_setup = time.time()
+    w13, w13s, w2, w2s = device_weights(device)
+    ctx = moe.MoE(H, I, E, K, max(SWEEP_T + [args.tokens]), device=local)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    log("setup %.1fs" % (time.time() - t_setup))
+
+    def fwd(xd, idd, wd, out):
+        ctx.forward(xd, idd, wd, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out)
+
+    def timed_loop(T, steps, warmup):
+        x, ids, w, xd, idd, wd = batch(T, device)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        for _ in range(warmup):
+            flush.zero_()
+            fwd(xd, idd, wd, out)
+        torch.cuda.synchronize(device)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(pg)
+        torch.cuda.synchronize(device)
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fwd(xd, idd, wd, out)
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(pg)
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return ms, out
+
+    # --- clocks: sampled over a soak + the timed region + a soak
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    t_soak = time.time()
+    soak_until = t_soak + args.soak
+    xs_, ids_, ws_, xd_, idd_, wd_ = batch(HEAD_T, device)
+    out_soak = torch.empty((HEAD_T, H), dtype=torch.bfloat16, device=device)
+    while time.time() < soak_until:
+        for _ in range(20):
+            fwd(xd_, idd_, wd_, out_soak)
+        torch.cuda.synchronize(device)
+
+    t0 = time.time()
+    ms, _ = timed_loop(args.tokens, args.steps, args.warmup)
+    t1 = time.time()
+    soak_until = time.time() + args.soak
+    while time.time() < soak_until:
+        for _ in range(20):
+            fwd(xd_, idd_, wd_, out_soak)
+        torch.cuda.synchronize(device)
+    t2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_soak, t2)
+
+    step_ms = statistics.mean(ms)
+    step_ms_max = max_over_ranks(pg, step_ms, device)
+    value_us = step_ms_max * 1000.0 / world  # whole job: calls of all ranks over the slowest rank's time
+
+    # --- per-kernel breakdown (separate, profiled pass)
+    ctx.set_profiling(True)
+    x, ids, w, xd, idd, wd = batch(args.tokens, device)
+    out = torch.empty((args.tokens, H), dtype=torch.bfloat16, device=device)
+    per = {}
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        fwd(xd, idd, wd, out)
+        prof = ctx.read_profile()
+        if i >= args.warmup:
+            for name, t in prof:
+                per.setdefault(name, []).append(t)
+    ctx.set_profiling(False)
+    per_avg = {k: statistics.mean(v) for k, v in per.items()}
+    srt = ctx.last_sort()
+    n_active = srt["num_active"]
+    n_pairs = int((srt["sorted_ids"] < args.tokens * K).sum().item())
+    ab = algo_bytes(args.tokens, n_active, n_pairs)
+    dominant = max(("stage1", "stage2"), key=lambda k: per_avg.get(k, 0.0))
+    peak, peak_kind = measured_peaks()
+    achieved = ab[dominant] / (per_avg[dominant] * 1e-3) / 1e9
+    traffic = stored_traffic(dominant, args.tokens)
+
+    # --- sweep over the decode token tiers
+    sweep = {}
+    for T in SWEEP_T:
+        ms_t, _ = timed_loop(T, max(10, args.steps // 2), 3)
+        sweep[str(T)] = round(statistics.mean(ms_t) * 1000.0, 2)
+
+    # --- end to end through the host-buffer API (pinned host memory)
+    x_h = x.pin_memory()
+    ids_h = ids.pin_memory()
+    w_h = w.pin_memory()
+    out_h = torch.empty((args.tokens, H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(args.warmup):
+        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out_h)
+    e2e = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(device)
+        ts = time.perf_counter()
+        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out_h)
+        e2e.append((time.perf_counter() - ts) * 1e6)
+    e2e_us = max_over_ranks(pg, statistics.mean(e2e), device) / world
+    st, flags = ctx.get_error()
+    if st != 0:
+        log("device error flags: %d" % flags)
+
+    result = {
+        "metric": "fused-MoE us/call and % roofline vs tokens (3584x384, 896 experts, top-16)",
+        "value": round(value_us, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": round(value_us / PAGE_US_A16W4[args.tokens], 4) if args.tokens in PAGE_US_A16W4 else None,
+        "dtype": "e2m1 x bf16 (re-encoded f16), fp32 accumulate",
+        "data": "synthetic (seeded; weights drawn on the GPU and MXFP4-quantised by the library)",
+        "config": {"workload": "Kimi-K3 TP8-shard decode a16w4: hidden 3584, inter 384, 896 experts, top-16 uniform, "
+                               "SiTUv2 beta 4 / linear beta 25, bf16 out, seed 123",
+                   "tokens": args.tokens, "a_dtype": "bf16", "act": "situv2",
+                   "l2": "flushed before every timed step (256 MB memset, outside the events)",
+                   "active_experts": n_active, "routed_pairs": n_pairs,
+                   "sweep_us_per_call": sweep, "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algo_bytes_per_launch": ab[dominant],
+                     "call_frac": round(ab["call"] / (step_ms * 1e-3) / 1e9 / peak, 4),
+                     "kernel_ms": {k: round(v, 5) for k, v in per_avg.items()}},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
+                "h2d_bytes_per_step": args.tokens * H * 2 + args.tokens * K * 8,
+                "d2h_bytes_per_step": args.tokens * H * 2},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.tokens, args.cpu_sample)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_inputs(T, sample):
+    import oracle
+    x = inputs.make_x(T, H, SEED)
+    ids, w = inputs.make_routing(T, E, K, "uniform", SEED)
+    sub = np.arange(min(sample, T), dtype=np.int32)
+    experts = np.unique(ids.numpy()[sub])
+    w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
+    w13s = np.zeros((E, 2 * I, H // 32), np.uint8)
+    w2 = np.zeros((E, H, I // 2), np.uint8)
+    w2s = np.zeros((E, H, I // 32), np.uint8)
+    for e in experts:
+        w13[e], w13s[e] = oracle.quantize_weights(inputs.expert_w13(int(e), H, I, SEED).numpy())
+        w2[e], w2s[e] = oracle.quantize_weights(inputs.expert_w2(int(e), H, I, SEED).numpy())
+    xb = x.view(torch.int16).numpy().astype(np.uint16)
+    return xb, ids.numpy(), w.numpy(), w13, w13s, w2, w2s, sub
+
+
+def _oracle_step(args_in):
+    import oracle
+    xb, ids, w, w13, w13s, w2, w2s, sub = args_in
+    t = time.perf_counter()
+    oracle.moe_forward(xb, ids, w, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", subset=sub)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(T, sample):
+    import oracle
+    data = _oracle_inputs(T, sample)
+    dt = _oracle_step(data)
+    n = len(data[-1])
+    return {"value": round(dt / n * T * 1e6, 1), "unit": "us/call", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of the %d tokens of the T=%d batch (all their %d routed pairs), one timed oracle call, "
+                      "scaled by T/%d" % (n, T, T, n * K, n)}
+
+
+def run_reference(args, world, rank, local, pg):
+    import oracle
+    if rank != 0:
+        return None
+    data = _oracle_inputs(args.tokens, args.ref_sample)
+    n = len(data[-1])
+    for _ in range(args.warmup):
+        _oracle_step(data)
+    ts = [_oracle_step(data) for _ in range(args.steps)]
+    us = statistics.mean(ts) / n * args.tokens * 1e6
+    sample = ("%d of the %d tokens per step (all their routed pairs), scaled by T/%d; fp64 CPU oracle"
+              % (n, args.tokens, n))
+    return {
+        "impl": "reference",
+        "metric": "fused-MoE us/call and % roofline vs tokens (3584x384, 896 experts, top-16)",
+        "value": round(us, 1), "unit": "us/call", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; weights quantised by the oracle)",
+        "config": {"workload": "Kimi-K3 TP8-shard decode a16w4: hidden 3584, inter 384, 896 experts, top-16 uniform, "
+                               "SiTUv2 beta 4 / linear beta 25, bf16 out, seed 123", "tokens": args.tokens},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=HEAD_T)
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps around the timed region")
+    ap.add_argument("--cpu-sample", type=int, default=16)
+    ap.add_argument("--ref-sample", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local, pg = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank, local, pg)
+    else:
+        res = run_ours(args, world, rank, local, pg)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) two-stage quantized MoE expert computation.
+ *
+ * The operation (from the ROCm/aiter pull-request pages this library follows):
+ *   - "Retune Kimi-K3 a16w4 MoE tile geometry" (aiter PR 5118), Summary:
+ *     moe_sorting groups the routed (token, k) pairs by expert and pads every
+ *     expert to a full tile of rows; stage 2 applies the top-k weight and
+ *     scatters each row back to its token.
+ *   - "Add an opt-in a4w4 SiTUv2 MoE path and fix three SiTUv2 tuner defects"
+ *     (aiter PR 4463), What: the activation dtype is bf16 (a16w4), fp8 (a8w4)
+ *     or fp4x2 (a4w4); weights are MXFP4 (e2m1 codes, two per byte, with an
+ *     e8m0 scale per 32 elements along K).
+ *   - "Add Kimi-K3 A8W4 support to the FlyDSL MegaMoE V2 operator" (aiter PR
+ *     6259), Motivation: SiTUv2, situ(g) = beta*tanh(g/beta)*sigmoid(g),
+ *     up = lbeta*tanh(u/lbeta), y = situ(g)*up, with beta = 4, lbeta = 25 for
+ *     Kimi-K3; Technical Details: SiTUv2 in the stage-1 epilogue, 1x32
+ *     blockwise fp8 quantisation.
+ *   - "Support SiTUv2 in the packed-int4 MoE stage1 epilogue" (aiter PR 4471),
+ *     Motivation: SiLU is y = silu(g)*u; an unsupported activation must be
+ *     rejected instead of silently computing SiLU.
+ *
+ * For each token t and each of its K routed experts e = topk_ids[t,k]:
+ *   a      = x[t] (bf16) or x[t] quantised to fp8/fp4 with 1x32 e8m0 scales
+ *   g_j    = a . W13[e, j, :],  u_j = a . W13[e, I+j, :]      (j < I)
+ *   y_j    = act(g_j, u_j), then requantised: bf16 (a16) or fp8/fp4 1x32 along I
+ *   z_h    = y . W2[e, h, :]                                   (h < H)
+ *   out[t] = bf16( sum_k topk_weights[t,k] * z )   (fp32 sum, one rounding)
+ *
+ * Layouts (all row-major, K contiguous; plain, not pre-swizzled):
+ *   x            bf16   [T, H]
+ *   topk_ids     int32  [T, K]   expert ids; ids outside [0,E) are dropped and
+ *                                flagged (moe_get_error); duplicates are legal
+ *   topk_weights fp32   [T, K]
+ *   w13          uint8  [E, 2I, H/2]  e2m1 codes; rows 0..I-1 gate, I..2I-1 up;
+ *                                     byte j of a row = element 2j (low nibble),
+ *                                     element 2j+1 (high nibble)
+ *   w13_scale    uint8  [E, 2I, H/32] e8m0 scales
+ *   w2           uint8  [E, H, I/2]
+ *   w2_scale     uint8  [E, H, I/32]
+ *   out          bf16   [T, H]   overwritten
+ *
+ * Ownership: every tensor argument is a caller-owned device pointer (16-byte
+ * aligned) unless the function says "host". The context owns its workspace
+ * (sort buffers, quantised activations, intermediate, fp32 combine buffer),
+ * sized once at moe_create for max_tokens. moe_forward and moe_sort allocate
+ * nothing and never synchronise the stream; they only enqueue kernels.
+ *
+ * Errors: argument checks run on the host before anything is enqueued and
+ * return a status; no C++ exception crosses this ABI. A CUDA launch error
+ * returns MOE_ERR_CUDA (text in moe_last_error_message()). Conditions found on
+ * the device (bad expert ids, a bounded wait that ran out) set bits of a
+ * device error word read by moe_get_error.
+ *
+ * Requirements: a GPU of compute capability 10.3 (GB300); hidden and inter
+ * multiples of 128; 1 <= num_experts <= 4096.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, T > max_tokens, beta <= 0 ... */
+  MOE_ERR_UNSUPPORTED = 2,   /* unknown activation or dtype, wrong GPU, shape outside the limits */
+  MOE_ERR_CUDA = 3,          /* a CUDA call failed */
+  MOE_ERR_OOM = 4,           /* workspace allocation failed in moe_create */
+  MOE_ERR_BAD_EXPERT_ID = 5, /* reported by moe_get_error's return: ids outside [0,E) were dropped */
+  MOE_ERR_TIMEOUT = 6        /* reported by moe_get_error's return: a device wait ran out */
+} moe_status;
+
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SITUV2 = 1 } moe_act;
+typedef enum { MOE_A_BF16 = 0, MOE_A_FP8 = 1, MOE_A_FP4 = 2 } moe_adtype;
+
+/* Device error word bits (moe_get_error). */
+#define MOE_DEVERR_BAD_EXPERT 1
+#define MOE_DEVERR_TIMEOUT 2
+#define MOE_DEVERR_OVERFLOW 4
+
+/* Sort output: device pointers into the context's workspace, valid until the
+ * next call on the same context. Sizes are upper bounds; the real counts live
+ * on the device in meta = {num_blocks, num_active, num_rows}.
+ * ("Retune Kimi-K3 a16w4 MoE tile geometry", Summary: moe_sorting pads every
+ * expert up to a full block_m.) */
+typedef struct {
+  int32_t* sorted_ids;     /* [max_rows]   pair id p = t*K+k per row; padding rows hold T*K */
+  int32_t* block_expert;   /* [max_blocks] expert of each tile_m block, ascending */
+  int32_t* expert_count;   /* [E]          valid pairs per expert */
+  int32_t* expert_offset;  /* [E+1]        first row of each expert; expert_offset[E] = num_rows */
+  int32_t* active_experts; /* [E]          experts with a nonzero count, ascending */
+  int32_t* meta;           /* [4]          num_blocks, num_active, num_rows, (reserved) */
+  int32_t tile_m;
+  int64_t max_rows;
+  int64_t max_blocks;
+} moe_sort_view;
+
+/* Workspace view for inspection (tests, debugging): device pointers owned by ctx.
+ * inter_codes rows follow the sorted order; its element format is that of the
+ * last moe_forward's a_dtype: bf16 path -> f16 codes (2 bytes, block-scaled
+ * re-encoding of the bf16 intermediate), fp8 -> e4m3 bytes, fp4 -> e2m1 pairs. */
+typedef struct {
+  moe_sort_view sort;
+  uint8_t* act_codes;      /* [max_tokens, H * bytes/elt] */
+  uint8_t* act_scales;     /* [max_tokens, H/32] */
+  uint8_t* inter_codes;    /* [max_rows, I * bytes/elt] */
+  uint8_t* inter_scales;   /* [max_rows, I/32] */
+  float* acc32;            /* [max_tokens, H] fp32 combine buffer */
+} moe_workspace_view;
+
+/* Create a context on `device` for fixed (hidden, inter, num_experts, topk) and
+ * up to max_tokens tokens per call. Allocates the whole workspace once.
+ * Returns MOE_ERR_UNSUPPORTED if the device is not compute capability 10.3 or
+ * a size is outside the limits above, MOE_ERR_OOM if allocation fails. */
+moe_status moe_create(moe_ctx** ctx, int hidden, int inter, int num_experts, int topk, int max_tokens, int device);
+
+/* Free the context and its workspace (synchronises its device). NULL is a no-op. */
+moe_status moe_destroy(moe_ctx* ctx);
+
+/* The expert sort alone (S1): bucket the num_tokens*topk pairs of topk_ids
+ * (device int32 [T,K]) by expert, ascending pair id inside an expert, each
+ * non-empty expert padded to a multiple of tile_m (1..256, a power of two) with
+ * the sentinel T*K. Fills *out with pointers into ctx's workspace. Enqueued on
+ * `stream` (a cudaStream_t; NULL = legacy default stream). */
+moe_status moe_sort(moe_ctx* ctx, const int32_t* topk_ids, int num_tokens, int tile_m, moe_sort_view* out,
+                    void* stream);
+
+/* The whole two-stage forward pass (sort, activation quantisation, stage 1,
+ * stage 2, combine) for num_tokens tokens, enqueued on `stream`. act and
+ * a_dtype are the moe_act / moe_adtype values; beta and linear_beta are always
+ * passed explicitly (no defaults; "Add an opt-in a4w4 SiTUv2 MoE path...",
+ * Three tuner defects item 1) and must be finite and > 0; SiLU ignores them.
+ * out (bf16 [T,H]) is overwritten. */
+moe_status moe_forward(moe_ctx* ctx, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                       int num_tokens, const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
+                       const uint8_t* w2_scale, int act, float beta, float linear_beta, int a_dtype, void* out,
+                       void* stream);
+
+/* moe_forward with HOST buffers for the per-call data: x_host (bf16 [T,H]),
+ * topk_ids_host, topk_weights_host and out_host (bf16 [T,H]) live in host
+ * memory (pinned memory makes the copies asynchronous); the weights are device
+ * pointers. Copies the inputs into ctx-owned device staging, runs moe_forward,
+ * copies the result back and synchronises `stream` before returning. */
+moe_status moe_forward_host(moe_ctx* ctx, const void* x_host, const int32_t* topk_ids_host,
+                            const float* topk_weights_host, int num_tokens, const uint8_t* w13,
+                            const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale, int act,
+                            float beta, float linear_beta, int a_dtype, void* out_host, void* stream);
+
+/* Activation block quantisation alone (S2): x bf16 [T,H] (device) -> codes and
+ * e8m0 scales per 32 along H, the operand format stage 1 reads. a_dtype
+ * MOE_A_FP8: e4m3 codes [T,H]; MOE_A_FP4: e2m1 pairs [T,H/2]; MOE_A_BF16: the
+ * bf16 values re-encoded as block-scaled f16 [T,H] (2 bytes each). Scale rule
+ * (OCP MX): an all-zero block gets scale 127 and +0 codes, else
+ * E = floor(log2(amax)) - emax (2 for e2m1, 8 for e4m3, 15 for f16), clamped
+ * to [-127,127], scale byte E+127, code = RNE(v / 2^E) saturating.
+ * Needs no context. */
+moe_status moe_quantize_activations(const void* x, int num_tokens, int hidden, int a_dtype, uint8_t* codes,
+                                    uint8_t* scales, void* stream);
+
+/* MXFP4 weight quantisation: fp32 w [rows, cols] (device, cols % 32 == 0) ->
+ * e2m1 codes [rows, cols/2] + e8m0 scales [rows, cols/32] with the same rule.
+ * Needs no context. */
+moe_status moe_quantize_mxfp4(const float* w, int64_t rows, int cols, uint8_t* codes, uint8_t* scales,
+                              void* stream);
+
+/* Pointers into ctx's workspace (see moe_workspace_view). */
+moe_status moe_get_workspace(moe_ctx* ctx, moe_workspace_view* out);
+
+/* Synchronise ctx's device, read and clear the device error word.
+ * *device_flags receives MOE_DEVERR_* bits. Returns MOE_OK when no bit was
+ * set, else MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT (timeout wins). */
+moe_status moe_get_error(moe_ctx* ctx, int32_t* device_flags);
+
+/* Benchmark support: when enabled, each moe_forward records a CUDA event on
+ * its stream before every kernel launch (group) and after the last one, so
+ * that moe_read_profile can report per-kernel device time. Off by default. */
+moe_status moe_set_profiling(moe_ctx* ctx, int enable);
+
+/* After a profiled moe_forward: wait for its last event and return, in launch
+ * order, the device time in ms (ms[i]) and a static name (names[i]) of each
+ * launch group: "sort", "act_quant", "stage1", "stage2", "finalize".
+ * *count is the capacity on entry and the number written on return. */
+moe_status moe_read_profile(moe_ctx* ctx, float* ms, const char** names, int* count);
+
+/* Static text for a status. */
+const char* moe_status_string(moe_status s);
+
+/* Text of the last failing CUDA call or argument check on this thread. */
+const char* moe_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,267 @@
+// Device helpers shared by the MoE kernels (sm_103a).
+//
+// Formats follow the OCP MX definitions used on the aiter pages ("Add an opt-in
+// a4w4 SiTUv2 MoE path...", Three tuner defects item 2: fp4x2 packs two e2m1
+// codes per byte; "Add Kimi-K3 A8W4 support...", Technical Details: fp8 1x32
+// block scales). Activation operands of both GEMMs are "block-scaled codes":
+// a code array plus one e8m0 scale per 32 elements along K, with codes in one
+// of three element formats:
+//   FMT_F16  : IEEE half (the lossless re-encoding of bf16 values, a16 path)
+//   FMT_E4M3 : fp8 e4m3fn (a8 path)
+//   FMT_E2M1 : fp4 e2m1, two per byte, element 2j in the low nibble (a4 path)
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda.h>
+
+namespace moe {
+
+enum ActFmt : int { FMT_F16 = 0, FMT_E4M3 = 1, FMT_E2M1 = 2 };
+enum Act : int { ACT_SILU = 0, ACT_SITUV2 = 1 };
+
+// Device error word bits (read back by moe_get_error).
+enum : int {
+  DEV_ERR_BAD_EXPERT = 1,   // a routed expert id was outside [0, E); the pair was dropped
+  DEV_ERR_TIMEOUT = 2,      // a bounded wait ran out; the kernel returned early
+  DEV_ERR_OVERFLOW = 4,     // sorted rows would exceed the workspace; extra rows dropped
+};
+
+__device__ __forceinline__ void set_error(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Scale and element formats
+// ---------------------------------------------------------------------------
+
+// e8m0 byte -> 2^(s-127) as fp32 (s = 0 is the fp32 subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  uint32_t bits = (s == 0u) ? 0x00400000u : (s == 255u ? 0x7FC00000u : (s << 23));
+  return __uint_as_float(bits);
+}
+
+// floor(log2(a)) for a finite a > 0, exact, from the fp32 bits.
+__device__ __forceinline__ int floor_log2_f32(float a) {
+  uint32_t b = __float_as_uint(a);
+  int ef = (int)((b >> 23) & 0xFFu);
+  if (ef) return ef - 127;
+  return (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+}
+
+// 2^-E as fp32 for E in [-127, 127] (exact).
+__device__ __forceinline__ float exp2_neg(int E) {
+  int f = 127 - E;  // in [0, 254]
+  return __uint_as_float(f == 0 ? 0x00400000u : ((uint32_t)f << 23));
+}
+
+// Largest normal exponent of each element format: the MX scale rule sets
+// E = floor(log2(amax)) - emax so that the block maximum lands in the top binade.
+__device__ __forceinline__ int fmt_emax(int fmt) { return fmt == FMT_E2M1 ? 2 : (fmt == FMT_E4M3 ? 8 : 15); }
+
+// Two fp32 -> packed e2m1x2 (RNE, saturating). lo -> low nibble, hi -> high nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t out;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n mov.b32 %0, {t, t, t, t};\n}"
+      : "=r"(out) : "f"(hi), "f"(lo));
+  return out & 0xFFu;
+}
+
+// Two fp32 -> packed e4m3x2 (RNE, saturating). lo -> low byte, hi -> high byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(hi), "f"(lo));
+  return (uint32_t)out;
+}
+
+// Eight e2m1 codes (nibble i = element i) -> four f16x2 words; word j holds
+// elements 2j (low half) and 2j+1 (high half).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+// Eight e2m1 codes (nibble i = element i) -> eight e4m3 bytes holding
+// 2^-6 * value, split into even and odd elements:
+//   even byte j = element 2j, odd byte j = element 2j+1.
+// e2m1 s.e1e0.m maps to e4m3 s.00e1e0.m00 (exponent field e1e0, top mantissa
+// bit m), whose value is exactly 2^-6 times the e2m1 value, subnormals included.
+__device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t w, uint32_t& even, uint32_t& odd) {
+  even = ((w << 2) & 0x1C1C1C1Cu) | ((w << 4) & 0x80808080u);
+  odd = ((w >> 2) & 0x1C1C1C1Cu) | (w & 0x80808080u);
+}
+
+// ---------------------------------------------------------------------------
+// Activation functions (aiter PR 6259 Motivation, PR 4471 Motivation)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta) {
+  float sig = 1.0f / (1.0f + __expf(-g));
+  if (act == ACT_SILU) return g * sig * u;
+  float situ = beta * tanhf(g / beta) * sig;
+  float up = lbeta * tanhf(u / lbeta);
+  return situ * up;
+}
+
+// ---------------------------------------------------------------------------
+// Warp helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Warp-cooperative 1x32 block quantisation: lane l holds element l of the block.
+// Returns the lane's code in the low bits (f16 bits / e4m3 byte / e2m1 nibble)
+// and the block's e8m0 scale byte in *scale. Rule: amax == 0 -> scale 127 and
+// +0 codes; else E = floor(log2 amax) - emax (clamped to [-127,127]) and
+// code = RNE(v * 2^-E), saturating.
+__device__ __forceinline__ uint32_t block_quant_lane(float v, int fmt, uint32_t* scale) {
+  float amax = warp_max(fabsf(v));
+  if (amax == 0.0f) {
+    *scale = 127u;
+    return 0u;
+  }
+  int E = floor_log2_f32(amax) - fmt_emax(fmt);
+  E = E < -127 ? -127 : (E > 127 ? 127 : E);
+  *scale = (uint32_t)(E + 127);
+  float q = __fmul_rn(v, exp2_neg(E));
+  if (fmt == FMT_F16) return (uint32_t)__half_as_ushort(__float2half_rn(q));
+  if (fmt == FMT_E4M3) return cvt_e4m3x2(q, 0.0f) & 0xFFu;
+  return cvt_e2m1x2(q, 0.0f) & 0xFu;
+}
+
+// Store one lane's code of a quantised 32-block: bytes per element 2 (f16),
+// 1 (e4m3) or 1/2 (e2m1, lanes pair up into bytes). dst points at the block.
+__device__ __forceinline__ void block_store_lane(uint8_t* dst, uint32_t code, int fmt, int lane) {
+  if (fmt == FMT_F16) {
+    reinterpret_cast<uint16_t*>(dst)[lane] = (uint16_t)code;
+  } else if (fmt == FMT_E4M3) {
+    dst[lane] = (uint8_t)code;
+  } else {
+    uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+    if ((lane & 1) == 0) dst[lane >> 1] = (uint8_t)(code | (nb << 4));
+  }
+}
+
+__device__ __forceinline__ int fmt_bytes_per_32(int fmt) { return fmt == FMT_F16 ? 64 : (fmt == FMT_E4M3 ? 32 : 16); }
+
+// ---------------------------------------------------------------------------
+// mbarrier / TMA (inline PTX). Every wait is bounded: on timeout it records
+// DEV_ERR_TIMEOUT and returns false, so no kernel can spin forever.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// ~2^22 polls with back-off: several seconds at most.
+#ifndef MOE_WAIT_LIMIT
+#define MOE_WAIT_LIMIT (1u << 22)
+#endif
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  for (uint32_t i = 0; i < MOE_WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
+  }
+  set_error(err, DEV_ERR_TIMEOUT);
+  return false;
+}
+
+// Wait that drains instead of hanging: once any thread of the CTA has timed
+// out (*abort set), every later wait returns false at once, so all warps run
+// to the end of their loops (meeting every named barrier) and the CTA exits.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
+  for (uint32_t i = 0; i < MOE_WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
+  }
+  *abort = 1;
+  set_error(err, DEV_ERR_TIMEOUT);
+  return false;
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int x, int y, int z, int w, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+               :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Register-operand MMA (m16n8, fp32 accumulate)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_e4m3_16832(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Swizzled byte offset inside a TMA tile whose rows are `row_bytes` long
+// (64 -> SWIZZLE_64B, 128 -> SWIZZLE_128B): the 16-byte chunk index is
+// XOR-ed with bits [7, 7+log2(row_bytes/16)) of the row's byte address.
+__device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uint32_t row_bytes) {
+  uint32_t addr = row * row_bytes;
+  uint32_t mask = row_bytes / 16 - 1;
+  return addr + (((chunk ^ (addr >> 7)) & mask) << 4);
+}
+
+}  // namespace moe

@@ -1,0 +1,69 @@
+// Internal interface between the C-ABI host code and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+namespace moe {
+
+// Sort output (device pointers). meta[] holds device-side counters.
+enum { META_NUM_BLOCKS = 0, META_NUM_ACTIVE = 1, META_NUM_ROWS = 2, META_WORDS = 4 };
+
+struct SortOut {
+  int32_t* sorted_ids;      // [cap_rows]   pair id p = t*K+k per sorted row, sentinel T*K on padding
+  int32_t* block_expert;    // [cap_blocks] expert of each tile_m block
+  int32_t* expert_count;    // [E]          valid pairs per expert
+  int32_t* expert_offset;   // [E+1]        first sorted row of each expert (padded prefix sum)
+  int32_t* active_experts;  // [E]          experts with count > 0, ascending
+  int32_t* meta;            // [META_WORDS] num_blocks, num_active, num_rows
+};
+
+constexpr int SORT_SMALL_MAX_PAIRS = 8192;  // single-CTA sort up to this many pairs
+constexpr int SORT_CHUNK = 4096;            // pairs per CTA in the multi-CTA sort
+constexpr int SORT_MAX_EXPERTS = 4096;      // shared-memory bound of the sort kernels
+
+size_t sort_small_smem(int E);
+cudaError_t prep_set_smem_limits();
+cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* hist,
+                        int hist_cap_chunks, int* err, cudaStream_t st);
+cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, float* acc32,
+                             int num_sms, cudaStream_t st);
+cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
+                                cudaStream_t st);
+cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
+
+// Parameters of the grouped stage kernels (decode family).
+struct StageParams {
+  // activation operand of this stage: block-scaled codes [rows, Kdim] + e8m0 [rows, Kdim/32]
+  const uint8_t* aq;
+  const uint8_t* as;
+  // weight scales [E, Ndim, Kdim/32]
+  const uint8_t* wscale;
+  // sort output
+  const int32_t* sorted_ids;
+  const int32_t* expert_offset;
+  const int32_t* expert_count;
+  const int32_t* active_experts;
+  const int32_t* meta;
+  // stage-1 output (intermediate) or stage-2 combine target
+  uint8_t* oq;        // stage 1: [rows, I] codes
+  uint8_t* os;        // stage 1: [rows, I/32] scales
+  float* acc32;       // stage 2: [T, H]
+  const float* topk_w;  // stage 2: [T*K]
+  int T, H, I, E, K;
+  int act;
+  float beta, lbeta;
+  int* err;
+};
+
+constexpr int DEC_TOK = 8;       // tokens per MMA column group (mma n8)
+constexpr int DEC_STAGES = 8;    // weight pipeline depth (4 KB per stage)
+
+cudaError_t decode_set_smem_limits();
+int decode_s1_blocks_per_sm(int fmt, int H);
+int decode_s2_blocks_per_sm(int fmt, int I);
+cudaError_t launch_decode_stage1(int fmt, const StageParams& p, const CUtensorMap& tm_w13, int grid, cudaStream_t st);
+cudaError_t launch_decode_stage2(int fmt, const StageParams& p, const CUtensorMap& tm_w2, int grid, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,341 @@
+// Expert sort, activation block quantisation, weight quantisation and the
+// bf16 finalize of the combine buffer.
+//
+// The sort follows "Retune Kimi-K3 a16w4 MoE tile geometry" (aiter PR 5118),
+// Summary: moe_sorting buckets the routed (token, k) pairs by expert and pads
+// every expert up to a full tile of rows. Within an expert, pairs keep
+// ascending pair id p = t*K + k; padding rows hold the sentinel T*K; blocks of
+// tile_m rows are listed in ascending expert order. It is integer work and is
+// bit-exact by construction: histogram -> scan -> placement whose rank inside
+// an expert is computed, not raced for.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Sort building blocks
+// ---------------------------------------------------------------------------
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* smem32, int* total) {
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem32[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? smem32[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem32[lane] = w;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  int before = (warp > 0 ? smem32[warp - 1] : 0) + x - v;
+  *total = smem32[nw - 1];
+  __syncthreads();
+  return before;
+}
+
+// Scan of padded per-expert counts: writes expert_count, expert_offset,
+// active list, meta, block_expert and the padding sentinels.
+// cnt[e] (shared) holds counts on entry; on exit cursor[e] = expert_offset[e].
+__device__ void sort_scan_and_fill(const int* cnt, int* cursor, int E, int tile_m, int sentinel,
+                                   const SortOut& so, int* scan_smem) {
+  int per = (E + blockDim.x - 1) / blockDim.x;
+  int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int rows = 0, act = 0;
+  for (int e = e0; e < e1; ++e) {
+    int c = cnt[e];
+    rows += (c + tile_m - 1) / tile_m * tile_m;
+    act += c > 0;
+  }
+  int total_rows, total_act;
+  int row_base = block_exclusive_scan(rows, scan_smem, &total_rows);
+  int act_base = block_exclusive_scan(act, scan_smem, &total_act);
+  int off = row_base, ai = act_base;
+  for (int e = e0; e < e1; ++e) {
+    int c = cnt[e];
+    int padded = (c + tile_m - 1) / tile_m * tile_m;
+    so.expert_count[e] = c;
+    so.expert_offset[e] = off;
+    cursor[e] = off;
+    if (c > 0) so.active_experts[ai++] = e;
+    off += padded;
+  }
+  if (threadIdx.x == 0) {
+    so.expert_offset[E] = total_rows;
+    so.meta[META_NUM_BLOCKS] = total_rows / tile_m;
+    so.meta[META_NUM_ACTIVE] = total_act;
+    so.meta[META_NUM_ROWS] = total_rows;
+  }
+  __syncthreads();
+  // padding sentinels and per-block expert ids
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = cnt[e];
+    if (c == 0) continue;
+    int o = cursor[e];
+    int padded = (c + tile_m - 1) / tile_m * tile_m;
+    for (int r = o + c; r < o + padded; ++r) so.sorted_ids[r] = sentinel;
+    for (int b = o / tile_m; b < (o + padded) / tile_m; ++b) so.block_expert[b] = e;
+  }
+}
+
+// Stable placement of pairs [p0, p1) given cursor[e] = first free row of e.
+// Chunks of blockDim.x pairs in ascending order; inside a chunk the rank of a
+// pair among equal experts is (pairs of earlier warps, from a per-expert byte
+// table) + (earlier lanes of its warp, from __match_any_sync).
+__device__ void sort_place_range(const int32_t* ids, long p0, long p1, int E, int* cursor,
+                                 uint8_t* wtab /* [E][32] */, int32_t* sorted_ids) {
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned lt_mask = (1u << lane) - 1u;
+  for (long base = p0; base < p1; base += blockDim.x) {
+    long p = base + threadIdx.x;
+    int e = -1;
+    if (p < p1) {
+      int v = ids[p];
+      if (v >= 0 && v < E) e = v;
+    }
+    unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    int rank = __popc(peers & lt_mask);
+    int wcount = __popc(peers);
+    bool leader = (peers & lt_mask) == 0;
+    if (e >= 0 && leader) wtab[e * 32 + warp] = (uint8_t)wcount;
+    __syncthreads();
+    if (e >= 0) {
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(wtab + e * 32);
+      int prefix = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint32_t word = row[q];
+        int lo = q * 4;  // warps lo..lo+3
+        if (lo + 4 <= warp) {
+          prefix += __dp4a((int)word, 0x01010101, 0);
+        } else if (lo < warp) {
+          uint32_t keep = 0xFFFFFFFFu >> (8 * (4 - (warp - lo)));
+          prefix += __dp4a((int)(word & keep), 0x01010101, 0);
+        }
+      }
+      sorted_ids[cursor[e] + prefix + rank] = (int32_t)p;
+    }
+    __syncthreads();
+    if (e >= 0 && leader) {
+      wtab[e * 32 + warp] = 0;
+      atomicAdd(&cursor[e], wcount);
+    }
+    __syncthreads();
+  }
+}
+
+// Single-CTA sort for small T*K (decode): histogram, scan, placement in one launch.
+__global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t* __restrict__ ids, int n, int E, int tile_m,
+                                                          SortOut so, int* err) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* cnt = reinterpret_cast<int*>(smem);                // [E]
+  int* cursor = cnt + E;                                  // [E]
+  int* scan_smem = cursor + E;                            // [32]
+  uint8_t* wtab = reinterpret_cast<uint8_t*>(scan_smem + 32);  // [E][32]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(wtab)[i] = 0u;
+  __syncthreads();
+  bool bad = false;
+  for (int p = threadIdx.x; p < n; p += blockDim.x) {
+    int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) set_error(err, DEV_ERR_BAD_EXPERT);
+  __syncthreads();
+  sort_scan_and_fill(cnt, cursor, E, tile_m, n, so, scan_smem);
+  __syncthreads();
+  sort_place_range(ids, 0, n, E, cursor, wtab, so.sorted_ids);
+}
+
+// Multi-CTA sort, pass 1: per-chunk histograms hist[g][e].
+__global__ void __launch_bounds__(1024) sort_hist_kernel(const int32_t* __restrict__ ids, long n, int E, int chunk,
+                                                         int* __restrict__ hist, int* err) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* cnt = reinterpret_cast<int*>(smem);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  long p0 = (long)blockIdx.x * chunk, p1 = min(n, p0 + chunk);
+  bool bad = false;
+  for (long p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad) set_error(err, DEV_ERR_BAD_EXPERT);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(long)blockIdx.x * E + e] = cnt[e];
+}
+
+// Multi-CTA sort, pass 2 (one CTA): totals, scan, fill; hist[g][e] becomes the
+// first row of chunk g's pairs of expert e.
+__global__ void __launch_bounds__(1024) sort_scan_kernel(int* __restrict__ hist, int G, int E, int tile_m, int sentinel,
+                                                         SortOut so) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* cnt = reinterpret_cast<int*>(smem);
+  int* cursor = cnt + E;
+  int* scan_smem = cursor + E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int g = 0; g < G; ++g) s += hist[(long)g * E + e];
+    cnt[e] = s;
+  }
+  __syncthreads();
+  sort_scan_and_fill(cnt, cursor, E, tile_m, sentinel, so, scan_smem);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = cursor[e];
+    for (int g = 0; g < G; ++g) {
+      int c = hist[(long)g * E + e];
+      hist[(long)g * E + e] = run;
+      run += c;
+    }
+  }
+}
+
+// Multi-CTA sort, pass 3: stable placement of each chunk.
+__global__ void __launch_bounds__(1024) sort_place_kernel(const int32_t* __restrict__ ids, long n, int E, int chunk,
+                                                          const int* __restrict__ hist, int32_t* sorted_ids) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* cursor = reinterpret_cast<int*>(smem);
+  uint8_t* wtab = reinterpret_cast<uint8_t*>(cursor + E);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = hist[(long)blockIdx.x * E + e];
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(wtab)[i] = 0u;
+  __syncthreads();
+  long p0 = (long)blockIdx.x * chunk, p1 = min(n, p0 + chunk);
+  sort_place_range(ids, p0, p1, E, cursor, wtab, sorted_ids);
+}
+
+// ---------------------------------------------------------------------------
+// Activation block quantisation (S2): x bf16 [T,H] -> codes + e8m0 scales per
+// 32 along H ("Add an opt-in a4w4 SiTUv2 MoE path...", What: a8w4 = fp8,
+// a4w4 = fp4x2 activations; 1x32 scales). FMT_F16 is the a16 operand: the
+// same bf16 values re-encoded as block-scaled f16 (exact for every element no
+// more than 2^31 below its block's maximum). Also zeroes the fp32 combine
+// buffer acc32 [T,H] for the stage-2 scatter that follows.
+// One warp per (token, 32-block); lane l handles element l.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int fmt,
+                                                        uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                                                        float* __restrict__ acc32) {
+  int lane = threadIdx.x & 31;
+  long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int nb = H / 32;
+  int bpb = fmt_bytes_per_32(fmt);
+  for (long blk = gw; blk < (long)T * nb; blk += nwarps) {
+    long t = blk / nb;
+    int b = (int)(blk % nb);
+    float v = __bfloat162float(x[t * H + b * 32 + lane]);
+    uint32_t s;
+    uint32_t code = block_quant_lane(v, fmt, &s);
+    block_store_lane(xq + (t * nb + b) * bpb, code, fmt, lane);
+    if (lane == 0) xs[t * nb + b] = (uint8_t)s;
+  }
+  if (acc32) {
+    long n4 = (long)T * H / 4;
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
+      reinterpret_cast<float4*>(acc32)[i] = z;
+  }
+}
+
+// MXFP4 weight quantisation: fp32 [rows, cols] -> e2m1 codes [rows, cols/2] +
+// e8m0 scales [rows, cols/32], the same 1x32 rule as the activations.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const float* __restrict__ w, long nblocks,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  int lane = threadIdx.x & 31;
+  long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  for (long blk = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < nblocks; blk += nwarps) {
+    float v = w[blk * 32 + lane];
+    uint32_t s;
+    uint32_t code = block_quant_lane(v, FMT_E2M1, &s);
+    block_store_lane(codes + blk * 16, code, FMT_E2M1, lane);
+    if (lane == 0) scales[blk] = (uint8_t)s;
+  }
+}
+
+// out = bf16_RNE(acc32), 4 elements per thread.
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc32, long n4, __nv_bfloat16* __restrict__ out) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x) {
+    float4 v = reinterpret_cast<const float4*>(acc32)[i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&a);
+    o.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(out)[i] = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers
+// ---------------------------------------------------------------------------
+size_t sort_small_smem(int E) { return (size_t)E * 8 + 32 * 4 + (size_t)E * 32; }
+
+cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* hist, int hist_cap_chunks,
+                        int* err, cudaStream_t st) {
+  if (n <= SORT_SMALL_MAX_PAIRS) {
+    sort_small_kernel<<<1, 1024, sort_small_smem(E), st>>>(ids, (int)n, E, tile_m, so, err);
+    return cudaGetLastError();
+  }
+  int chunk = SORT_CHUNK;
+  int G = (int)((n + chunk - 1) / chunk);
+  if (G > hist_cap_chunks) return cudaErrorInvalidValue;
+  sort_hist_kernel<<<G, 1024, (size_t)E * 4, st>>>(ids, n, E, chunk, hist, err);
+  sort_scan_kernel<<<1, 1024, (size_t)E * 8 + 32 * 4, st>>>(hist, G, E, tile_m, (int)n, so);
+  sort_place_kernel<<<G, 1024, (size_t)E * 4 + (size_t)E * 32, st>>>(ids, n, E, chunk, hist, so.sorted_ids);
+  return cudaGetLastError();
+}
+
+cudaError_t prep_set_smem_limits() {
+  cudaError_t e = cudaFuncSetAttribute(sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sort_small_smem(SORT_MAX_EXPERTS));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sort_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)((size_t)SORT_MAX_EXPERTS * 36));
+  return e;
+}
+
+cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, float* acc32, int num_sms,
+                             cudaStream_t st) {
+  long work = (long)T * (H / 32);
+  long blocks = (work + 7) / 8;
+  long cap = (long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  act_quant_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, fmt, xq, xs, acc32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
+                                cudaStream_t st) {
+  long blocks = (nblocks + 7) / 8;
+  long cap = (long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  weight_quant_kernel<<<(int)blocks, 256, 0, st>>>(w, nblocks, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st) {
+  long n4 = n / 4;
+  long blocks = (n4 + 255) / 256;
+  long cap = (long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  finalize_kernel<<<(int)blocks, 256, 0, st>>>(acc32, n4, reinterpret_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

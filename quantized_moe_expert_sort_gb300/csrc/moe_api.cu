@@ -1,0 +1,440 @@
+// C-ABI host library: argument checks, workspace ownership, tensor maps and
+// the launch sequence of the forward pass. See include/moe.h for the contract.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(call)                                   \
+  do {                                                   \
+    cudaError_t _e = (call);                             \
+    if (_e != cudaSuccess) return cuda_fail(_e, #call);  \
+  } while (0)
+
+constexpr int kMaxTile = 256;       // largest tile_m the sort accepts
+constexpr int kDecodeTile = DEC_TOK;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fmt_of_adtype(int a) { return a == MOE_A_BF16 ? FMT_F16 : (a == MOE_A_FP8 ? FMT_E4M3 : FMT_E2M1); }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+struct moe_ctx {
+  int H, I, E, K, max_tokens, device, num_sms;
+  long cap_rows, cap_blocks;
+  int hist_chunks;
+  int32_t *sorted_ids, *block_expert, *expert_count, *expert_offset, *active_experts, *meta, *hist;
+  uint8_t *xq, *xs, *inter_q, *inter_s;
+  float* acc32;
+  int* err;
+  void* st_x;
+  int32_t* st_ids;
+  float* st_w;
+  void* st_out;
+  int s1_bps[3], s2_bps[3];
+  const void* tm_w13_key;
+  CUtensorMap tm_w13;
+  const void* tm_w2_key;
+  CUtensorMap tm_w2;
+  int last_tile_m;
+  // profiling (moe_set_profiling)
+  int profiling;
+  cudaEvent_t ev[8];
+  const char* ev_name[8];
+  int ev_n;
+};
+
+static void prof_mark(moe_ctx* c, cudaStream_t st, const char* name) {
+  if (!c->profiling || c->ev_n >= 7) return;
+  cudaEventRecord(c->ev[c->ev_n], st);
+  c->ev_name[c->ev_n] = name;
+  ++c->ev_n;
+}
+
+static void free_ctx(moe_ctx* c) {
+  void* ptrs[] = {c->sorted_ids, c->block_expert, c->expert_count, c->expert_offset, c->active_experts,
+                  c->meta, c->hist, c->xq, c->xs, c->inter_q, c->inter_s, c->acc32, c->err,
+                  c->st_x, c->st_ids, c->st_w, c->st_out};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  for (cudaEvent_t e : c->ev)
+    if (e) cudaEventDestroy(e);
+  delete c;
+}
+
+static moe_status make_w13_map(moe_ctx* c, const uint8_t* w13) {
+  if (c->tm_w13_key == w13) return MOE_OK;
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[4] = {(cuuint64_t)c->H / 2, (cuuint64_t)c->I, 2, (cuuint64_t)c->E};
+  cuuint64_t strides[3] = {(cuuint64_t)c->H / 2, (cuuint64_t)c->I * c->H / 2, (cuuint64_t)2 * c->I * c->H / 2};
+  cuuint32_t box[4] = {64, 32, 2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(&c->tm_w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(w13), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(w13) failed: %d", (int)r);
+  c->tm_w13_key = w13;
+  return MOE_OK;
+}
+
+static moe_status make_w2_map(moe_ctx* c, const uint8_t* w2) {
+  if (c->tm_w2_key == w2) return MOE_OK;
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)c->I / 2, (cuuint64_t)c->H, (cuuint64_t)c->E};
+  cuuint64_t strides[2] = {(cuuint64_t)c->I / 2, (cuuint64_t)c->H * c->I / 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(&c->tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(w2), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(w2) failed: %d", (int)r);
+  c->tm_w2_key = w2;
+  return MOE_OK;
+}
+
+static SortOut sort_out(moe_ctx* c) {
+  SortOut so;
+  so.sorted_ids = c->sorted_ids;
+  so.block_expert = c->block_expert;
+  so.expert_count = c->expert_count;
+  so.expert_offset = c->expert_offset;
+  so.active_experts = c->active_experts;
+  so.meta = c->meta;
+  return so;
+}
+
+static void fill_sort_view(moe_ctx* c, int tile_m, moe_sort_view* v) {
+  v->sorted_ids = c->sorted_ids;
+  v->block_expert = c->block_expert;
+  v->expert_count = c->expert_count;
+  v->expert_offset = c->expert_offset;
+  v->active_experts = c->active_experts;
+  v->meta = c->meta;
+  v->tile_m = tile_m;
+  v->max_rows = c->cap_rows;
+  v->max_blocks = c->cap_blocks;
+}
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id out of range (pairs dropped)";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error_message(void) { return g_msg; }
+
+moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens, int device) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "ctx out-pointer is NULL");
+  *out = nullptr;
+  if (H <= 0 || I <= 0 || E <= 0 || K <= 0 || max_tokens <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (H=%d I=%d E=%d K=%d max_tokens=%d)", H, I, E, K, max_tokens);
+  if (H % 128 || I % 128) return fail(MOE_ERR_UNSUPPORTED, "hidden and inter must be multiples of 128");
+  if (H > 16384 || I > 16384) return fail(MOE_ERR_UNSUPPORTED, "hidden and inter are limited to 16384");
+  if (E > SORT_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "num_experts is limited to %d", SORT_MAX_EXPERTS);
+  if ((long)max_tokens * K > (1L << 30)) return fail(MOE_ERR_UNSUPPORTED, "max_tokens * topk too large");
+  int ndev = 0;
+  CUDA_TRY(cudaGetDeviceCount(&ndev));
+  if (device < 0 || device >= ndev) return fail(MOE_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, ndev);
+  cudaDeviceProp prop;
+  CUDA_TRY(cudaGetDeviceProperties(&prop, device));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(MOE_ERR_UNSUPPORTED, "needs a compute capability 10.3 GPU (GB300), device %d is %d.%d", device,
+                prop.major, prop.minor);
+  CUDA_TRY(cudaSetDevice(device));
+
+  moe_ctx* c = new moe_ctx();
+  std::memset(c, 0, sizeof(*c));
+  c->H = H; c->I = I; c->E = E; c->K = K; c->max_tokens = max_tokens; c->device = device;
+  c->num_sms = prop.multiProcessorCount;
+  long pairs = (long)max_tokens * K;
+  c->cap_rows = pairs + (long)(E < pairs ? E : pairs) * (kMaxTile - 1);
+  c->cap_rows = (c->cap_rows + kMaxTile - 1) / kMaxTile * kMaxTile;
+  c->cap_blocks = c->cap_rows;  // enough for tile_m = 1
+  c->hist_chunks = (int)((pairs + SORT_CHUNK - 1) / SORT_CHUNK);
+  if (c->hist_chunks < 1) c->hist_chunks = 1;
+
+  struct { void** p; size_t bytes; } allocs[] = {
+      {(void**)&c->sorted_ids, sizeof(int32_t) * c->cap_rows},
+      {(void**)&c->block_expert, sizeof(int32_t) * c->cap_blocks},
+      {(void**)&c->expert_count, sizeof(int32_t) * E},
+      {(void**)&c->expert_offset, sizeof(int32_t) * (E + 1)},
+      {(void**)&c->active_experts, sizeof(int32_t) * E},
+      {(void**)&c->meta, sizeof(int32_t) * META_WORDS},
+      {(void**)&c->hist, sizeof(int32_t) * (size_t)c->hist_chunks * E},
+      {(void**)&c->xq, (size_t)max_tokens * H * 2},
+      {(void**)&c->xs, (size_t)max_tokens * H / 32},
+      {(void**)&c->inter_q, (size_t)c->cap_rows * I * 2},
+      {(void**)&c->inter_s, (size_t)c->cap_rows * I / 32},
+      {(void**)&c->acc32, sizeof(float) * (size_t)max_tokens * H},
+      {(void**)&c->err, sizeof(int) * 4},
+      {(void**)&c->st_x, (size_t)max_tokens * H * 2},
+      {(void**)&c->st_ids, sizeof(int32_t) * pairs},
+      {(void**)&c->st_w, sizeof(float) * pairs},
+      {(void**)&c->st_out, (size_t)max_tokens * H * 2},
+  };
+  for (auto& a : allocs) {
+    cudaError_t e = cudaMalloc(a.p, a.bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      free_ctx(c);
+      return fail(MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", a.bytes, cudaGetErrorString(e));
+    }
+  }
+  cudaError_t e = cudaMemset(c->err, 0, sizeof(int) * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->meta, 0, sizeof(int32_t) * META_WORDS);
+  if (e == cudaSuccess) e = prep_set_smem_limits();
+  if (e == cudaSuccess) e = decode_set_smem_limits();
+  if (e != cudaSuccess) {
+    free_ctx(c);
+    return cuda_fail(e, "context setup");
+  }
+  for (int f = 0; f < 3; ++f) {
+    c->s1_bps[f] = decode_s1_blocks_per_sm(f, H);
+    c->s2_bps[f] = decode_s2_blocks_per_sm(f, I);
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+moe_status moe_destroy(moe_ctx* c) {
+  if (!c) return MOE_OK;
+  cudaSetDevice(c->device);
+  cudaDeviceSynchronize();
+  free_ctx(c);
+  return MOE_OK;
+}
+
+moe_status moe_get_workspace(moe_ctx* c, moe_workspace_view* v) {
+  if (!c || !v) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  fill_sort_view(c, c->last_tile_m, &v->sort);
+  v->act_codes = c->xq;
+  v->act_scales = c->xs;
+  v->inter_codes = c->inter_q;
+  v->inter_scales = c->inter_s;
+  v->acc32 = c->acc32;
+  return MOE_OK;
+}
+
+moe_status moe_sort(moe_ctx* c, const int32_t* ids, int T, int tile_m, moe_sort_view* out, void* stream) {
+  if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (T < 0 || T > c->max_tokens) return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", T, c->max_tokens);
+  if (tile_m < 1 || tile_m > kMaxTile || (tile_m & (tile_m - 1)))
+    return fail(MOE_ERR_INVALID_ARG, "tile_m must be a power of two in [1, %d]", kMaxTile);
+  if (T > 0 && !ids) return fail(MOE_ERR_INVALID_ARG, "topk_ids is NULL");
+  CUDA_TRY(cudaSetDevice(c->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_sort(ids, (long)T * c->K, c->E, tile_m, sort_out(c), c->hist, c->hist_chunks, c->err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sort launch");
+  c->last_tile_m = tile_m;
+  fill_sort_view(c, tile_m, out);
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const float* w, int T, const uint8_t* w13,
+                       const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act, float beta,
+                       float lbeta, int adt, void* out, void* stream) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (T < 0 || T > c->max_tokens) return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", T, c->max_tokens);
+  if (act != MOE_ACT_SILU && act != MOE_ACT_SITUV2) return fail(MOE_ERR_UNSUPPORTED, "activation %d is not silu or situv2", act);
+  if (adt != MOE_A_BF16 && adt != MOE_A_FP8 && adt != MOE_A_FP4) return fail(MOE_ERR_UNSUPPORTED, "a_dtype %d unknown", adt);
+  if (act == MOE_ACT_SITUV2 && !(beta > 0.0f && lbeta > 0.0f && beta < 3e38f && lbeta < 3e38f))
+    return fail(MOE_ERR_INVALID_ARG, "SiTUv2 needs finite beta > 0 and linear_beta > 0");
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, ids, w, w13, w13s, w2, w2s, out};
+  for (const void* p : ptrs) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  }
+  CUDA_TRY(cudaSetDevice(c->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int fmt = fmt_of_adtype(adt);
+  const long pairs = (long)T * c->K;
+  moe_status ms = make_w13_map(c, w13);
+  if (ms != MOE_OK) return ms;
+  ms = make_w2_map(c, w2);
+  if (ms != MOE_OK) return ms;
+
+  c->ev_n = 0;
+  prof_mark(c, st, "sort");
+  cudaError_t e = launch_sort(ids, pairs, c->E, kDecodeTile, sort_out(c), c->hist, c->hist_chunks, c->err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sort launch");
+  c->last_tile_m = kDecodeTile;
+  prof_mark(c, st, "act_quant");
+  e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, c->acc32, c->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+
+  StageParams p{};
+  p.sorted_ids = c->sorted_ids;
+  p.expert_offset = c->expert_offset;
+  p.expert_count = c->expert_count;
+  p.active_experts = c->active_experts;
+  p.meta = c->meta;
+  p.T = T; p.H = c->H; p.I = c->I; p.E = c->E; p.K = c->K;
+  p.act = act; p.beta = beta; p.lbeta = lbeta;
+  p.err = c->err;
+
+  const long max_active = pairs < c->E ? pairs : c->E;
+  StageParams p1 = p;
+  p1.aq = c->xq; p1.as = c->xs; p1.wscale = w13s;
+  p1.oq = c->inter_q; p1.os = c->inter_s;
+  long items1 = max_active * (c->I / 32);
+  long cap1 = (long)c->num_sms * c->s1_bps[fmt];
+  prof_mark(c, st, "stage1");
+  e = launch_decode_stage1(fmt, p1, c->tm_w13, (int)(items1 < cap1 ? items1 : cap1), st);
+  if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
+
+  StageParams p2 = p;
+  p2.aq = c->inter_q; p2.as = c->inter_s; p2.wscale = w2s;
+  p2.acc32 = c->acc32; p2.topk_w = w;
+  long items2 = max_active * (c->H / 64);
+  long cap2 = (long)c->num_sms * c->s2_bps[fmt];
+  prof_mark(c, st, "stage2");
+  e = launch_decode_stage2(fmt, p2, c->tm_w2, (int)(items2 < cap2 ? items2 : cap2), st);
+  if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
+
+  prof_mark(c, st, "finalize");
+  e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  prof_mark(c, st, "end");
+  return MOE_OK;
+}
+
+moe_status moe_forward_host(moe_ctx* c, const void* x_host, const int32_t* ids_host, const float* w_host, int T,
+                            const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act,
+                            float beta, float lbeta, int adt, void* out_host, void* stream) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (T < 0 || T > c->max_tokens) return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", T, c->max_tokens);
+  if (T == 0) return MOE_OK;
+  if (!x_host || !ids_host || !w_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "NULL host buffer");
+  CUDA_TRY(cudaSetDevice(c->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * c->H * 2, pb = (size_t)T * c->K;
+  CUDA_TRY(cudaMemcpyAsync(c->st_x, x_host, xb, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMemcpyAsync(c->st_ids, ids_host, pb * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMemcpyAsync(c->st_w, w_host, pb * sizeof(float), cudaMemcpyHostToDevice, st));
+  moe_status s = moe_forward(c, c->st_x, c->st_ids, c->st_w, T, w13, w13s, w2, w2s, act, beta, lbeta, adt,
+                             c->st_out, stream);
+  if (s != MOE_OK) return s;
+  CUDA_TRY(cudaMemcpyAsync(out_host, c->st_out, xb, cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+moe_status moe_quantize_activations(const void* x, int T, int H, int adt, uint8_t* codes, uint8_t* scales,
+                                    void* stream) {
+  if (T < 0 || H <= 0 || H % 32) return fail(MOE_ERR_INVALID_ARG, "bad sizes T=%d H=%d (H %% 32 == 0)", T, H);
+  if (adt != MOE_A_BF16 && adt != MOE_A_FP8 && adt != MOE_A_FP4) return fail(MOE_ERR_UNSUPPORTED, "a_dtype %d unknown", adt);
+  if (T == 0) return MOE_OK;
+  if (!x || !codes || !scales) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  cudaError_t e = launch_act_quant(x, T, H, fmt_of_adtype(adt), codes, scales, nullptr, sms,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+  return MOE_OK;
+}
+
+moe_status moe_quantize_mxfp4(const float* w, int64_t rows, int cols, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 32) return fail(MOE_ERR_INVALID_ARG, "bad sizes rows=%lld cols=%d", (long long)rows, cols);
+  if (rows == 0) return MOE_OK;
+  if (!w || !codes || !scales) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  cudaError_t e = launch_weight_quant(w, rows * (cols / 32), codes, scales, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "weight quantisation launch");
+  return MOE_OK;
+}
+
+moe_status moe_set_profiling(moe_ctx* c, int enable) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  CUDA_TRY(cudaSetDevice(c->device));
+  if (enable && !c->ev[0])
+    for (cudaEvent_t& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
+  c->profiling = enable ? 1 : 0;
+  c->ev_n = 0;
+  return MOE_OK;
+}
+
+moe_status moe_read_profile(moe_ctx* c, float* ms, const char** names, int* count) {
+  if (!c || !count) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!c->profiling || c->ev_n < 2) { *count = 0; return MOE_OK; }
+  CUDA_TRY(cudaEventSynchronize(c->ev[c->ev_n - 1]));
+  int n = c->ev_n - 1 < *count ? c->ev_n - 1 : *count;
+  for (int i = 0; i < n; ++i) {
+    float t = 0.f;
+    CUDA_TRY(cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]));
+    if (ms) ms[i] = t;
+    if (names) names[i] = c->ev_name[i];
+  }
+  *count = n;
+  return MOE_OK;
+}
+
+moe_status moe_get_error(moe_ctx* c, int32_t* flags) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  CUDA_TRY(cudaSetDevice(c->device));
+  CUDA_TRY(cudaDeviceSynchronize());
+  int v = 0;
+  CUDA_TRY(cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
+  if (flags) *flags = v;
+  if (v & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v & DEV_ERR_BAD_EXPERT) return MOE_ERR_BAD_EXPERT_ID;
+  return MOE_OK;
+}
+
+}  // extern "C"

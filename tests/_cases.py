@@ -1,0 +1,85 @@
+"""Test-case builder: seeded inputs (quantized_moe_expert_sort_gb300.inputs),
+MXFP4 weights quantised by the oracle, and helpers to compare with it."""
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+from quantized_moe_expert_sort_gb300 import inputs
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def bf16_bits(x):
+    return x.contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+
+def bits_to_f64(bits):
+    return torch.tensor(bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def quantized_experts(experts, H, I, seed, E):
+    """Oracle-quantised MXFP4 weights; experts not in `experts` stay zero
+    (never read by a routing that does not touch them)."""
+    w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
+    w13s = np.zeros((E, 2 * I, H // 32), np.uint8)
+    w2 = np.zeros((E, H, I // 2), np.uint8)
+    w2s = np.zeros((E, H, I // 32), np.uint8)
+    for e in sorted(set(int(v) for v in experts)):
+        c, s = oracle.quantize_weights(inputs.expert_w13(e, H, I, seed).numpy())
+        w13[e], w13s[e] = c, s
+        c, s = oracle.quantize_weights(inputs.expert_w2(e, H, I, seed).numpy())
+        w2[e], w2s[e] = c, s
+    return w13, w13s, w2, w2s
+
+
+@functools.lru_cache(maxsize=8)
+def _weights_cached(key, H, I, seed, E):
+    experts = np.frombuffer(key, dtype=np.int32)
+    return quantized_experts(experts, H, I, seed, E)
+
+
+def make_case(T, H, I, E, K, routing, seed, experts_all=False):
+    x = inputs.make_x(T, H, seed)
+    ids, w = inputs.make_routing(T, E, K, routing, seed)
+    ids_np = ids.numpy()
+    touched = np.arange(E, dtype=np.int32) if experts_all else np.unique(ids_np[(ids_np >= 0) & (ids_np < E)]).astype(np.int32)
+    w13, w13s, w2, w2s = _weights_cached(touched.tobytes(), H, I, seed, E)
+    return dict(x=x, x_bits=bf16_bits(x), ids=ids, w=w, w13=w13, w13s=w13s, w2=w2, w2s=w2s,
+                T=T, H=H, I=I, E=E, K=K)
+
+
+def oracle_forward(case, act, a_dtype, subset=None, want_inter=False, ids=None, w=None, beta=4.0, lbeta=25.0):
+    ids = case["ids"] if ids is None else ids
+    w = case["w"] if w is None else w
+    return oracle.moe_forward(case["x_bits"], np.asarray(ids), np.asarray(w), case["w13"], case["w13s"],
+                              case["w2"], case["w2s"], act, beta, lbeta, a_dtype, tile_m=16,
+                              subset=subset, want_inter=want_inter)
+
+
+def to_dev(case, device="cuda"):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return dict(x=case["x"].to(device), ids=case["ids"].to(device), w=case["w"].to(device),
+                w13=t(case["w13"]), w13s=t(case["w13s"]), w2=t(case["w2"]), w2s=t(case["w2s"]))
+
+
+def decode_codes(codes, scales, a_dtype):
+    """Decode GPU activation / intermediate codes to float64 (test-side decoder)."""
+    codes = np.asarray(codes)
+    scales = np.asarray(scales).astype(np.float64)
+    if a_dtype == "bf16":
+        v = codes.view(np.float16).astype(np.float64)
+    elif a_dtype == "fp8":
+        v = torch.tensor(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    else:
+        lo, hi = codes & 15, codes >> 4
+        c = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (codes.shape[-1] * 2,))
+        v = E2M1[c & 7] * np.where(c & 8, -1.0, 1.0)
+    return v * np.repeat(np.exp2(scales - 127), 32, axis=-1)
