@@ -130,6 +130,32 @@ moe_status moe_destroy(moe_ctx* ctx);
 moe_status moe_sort(moe_ctx* ctx, const int32_t* topk_ids, int num_tokens, int tile_m, moe_sort_view* out,
                     void* stream);
 
+/* Scratch of moe_sort_noalloc, in ints (a 1 MiB device array per GPU). */
+#define MOE_SORT_NOALLOC_SCRATCH_INTS 262144
+
+/* The expert sort of moe_sort, into buffers the caller passes, with no device
+ * memory allocated by this call or by any set-up it needs. The aiter pages
+ * have no counterpart: it serves callers of this library that cannot call
+ * cudaMalloc -- a serving engine whose memory pool owns the GPU's memory, a
+ * decode loop that must not risk the device synchronisation an allocation can
+ * cause, or a library that routes tokens without holding a moe_ctx.
+ * Runs on the calling thread's current device, enqueued on `stream`.
+ * Outputs (device, caller-owned; same meaning as moe_sort_view):
+ *   sorted_ids     [T*K + min(E, T*K)*(tile_m-1)]   block_expert [that / tile_m]
+ *   expert_count   [E]   expert_offset [E+1]   active_experts [E]
+ *   meta           [4]   num_blocks, num_active, num_rows, device flag bits
+ *                        (MOE_DEVERR_BAD_EXPERT when ids were dropped)
+ * Scratch: for T*K > 8192 the histogram rows, ceil(T*K/4096) * E ints, live in
+ * a file-scope device array of MOE_SORT_NOALLOC_SCRATCH_INTS ints; larger
+ * problems are rejected with MOE_ERR_INVALID_ARG (use moe_sort). Every call
+ * shares that array: calls whose kernels overlap on the GPU (different streams
+ * without ordering, or several host threads) race and must be serialised by
+ * the caller. The first call on a device looks up the array's device address
+ * and sets kernel attributes; make that first call before any stream capture. */
+moe_status moe_sort_noalloc(const int32_t* topk_ids, int num_tokens, int topk, int num_experts, int tile_m,
+                            int32_t* sorted_ids, int32_t* block_expert, int32_t* expert_count,
+                            int32_t* expert_offset, int32_t* active_experts, int32_t* meta, void* stream);
+
 /* The whole two-stage forward pass (sort, activation quantisation, stage 1,
  * stage 2, combine) for num_tokens tokens, enqueued on `stream`. act and
  * a_dtype are the moe_act / moe_adtype values; beta and linear_beta are always

@@ -24,6 +24,8 @@ constexpr int SORT_CHUNK = 4096;            // pairs per CTA in the multi-CTA so
 constexpr int SORT_MAX_EXPERTS = 4096;      // shared-memory bound of the sort kernels
 
 size_t sort_small_smem(int E);
+// Text returned by moe_last_error_message() on this thread.
+void set_last_error_message(const char* msg);
 cudaError_t prep_set_smem_limits();
 cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* hist,
                         int hist_cap_chunks, int* err, cudaStream_t st);

@@ -60,6 +60,8 @@ EncodeTiledFn get_encode_fn() {
 
 }  // namespace
 
+void moe::set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 struct moe_ctx {
   int H, I, E, K, max_tokens, device, num_sms;
   long cap_rows, cap_blocks;
