@@ -101,16 +101,23 @@ typedef struct {
 } moe_sort_view;
 
 /* Workspace view for inspection (tests, debugging): device pointers owned by ctx.
- * inter_codes rows follow the sorted order; its element format is that of the
- * last moe_forward's a_dtype: bf16 path -> f16 codes (2 bytes, block-scaled
- * re-encoding of the bf16 intermediate), fp8 -> e4m3 bytes, fp4 -> e2m1 pairs. */
+ * inter_codes rows follow the sorted order of the last moe_forward (tile_m 8 on
+ * the decode path, 128 on the tensor-core path); the element format is that of
+ * its a_dtype: bf16 -> f16 codes (2 bytes, block-scaled re-encoding of the bf16
+ * intermediate), fp8 -> e4m3 bytes, fp4 -> e2m1 pairs. */
 typedef struct {
   moe_sort_view sort;
   uint8_t* act_codes;      /* [max_tokens, H * bytes/elt] */
-  uint8_t* act_scales;     /* [max_tokens, H/32] */
+  uint8_t* act_scales;     /* [max_tokens, act_scale_stride] (first H/32 bytes of a row used) */
   uint8_t* inter_codes;    /* [max_rows, I * bytes/elt] */
-  uint8_t* inter_scales;   /* [max_rows, I/32] */
+  uint8_t* inter_scales;   /* [max_rows, inter_scale_stride] (first I/32 bytes of a row used) */
   float* acc32;            /* [max_tokens, H] fp32 combine buffer */
+  int32_t act_scale_stride;   /* H/32 rounded up to 16 */
+  int32_t inter_scale_stride; /* I/32 rounded up to 16 */
+  int32_t inter_scale_layout; /* 0: row-major [rows, inter_scale_stride];
+                                 1: per 128-row tile b and 4-block chunk c, 512 bytes at
+                                    (b * I/128 + c) * 512, byte 16*(m%32) + 4*(m/32) + kb%4
+                                    for tile row m and 32-block kb (tensor-core path) */
 } moe_workspace_view;
 
 /* Create a context on `device` for fixed (hidden, inter, num_experts, topk) and
@@ -179,11 +186,14 @@ moe_status moe_forward_host(moe_ctx* ctx, const void* x_host, const int32_t* top
 
 /* Activation block quantisation alone (S2): x bf16 [T,H] (device) -> codes and
  * e8m0 scales per 32 along H, the operand format stage 1 reads. a_dtype
- * MOE_A_FP8: e4m3 codes [T,H]; MOE_A_FP4: e2m1 pairs [T,H/2]; MOE_A_BF16: the
- * bf16 values re-encoded as block-scaled f16 [T,H] (2 bytes each). Scale rule
+ * MOE_A_FP8: e4m3 codes [T,H]; MOE_A_FP4: e2m1 pairs [T,H/2]. Scale rule
  * (OCP MX): an all-zero block gets scale 127 and +0 codes, else
- * E = floor(log2(amax)) - emax (2 for e2m1, 8 for e4m3, 15 for f16), clamped
- * to [-127,127], scale byte E+127, code = RNE(v / 2^E) saturating.
+ * E = floor(log2(amax)) - emax (2 for e2m1, 8 for e4m3), clamped to
+ * [-127,127], scale byte E+127, code = RNE(v / 2^E) saturating.
+ * MOE_A_BF16: the bf16 values re-encoded as IEEE half [T,H] (2 bytes each)
+ * times one power of two per token, E = floor(log2(row amax)) - 15, written
+ * into all H/32 scale bytes of the row; exact for every value no more than
+ * 2^31 below its row's maximum.
  * Needs no context. */
 moe_status moe_quantize_activations(const void* x, int num_tokens, int hidden, int a_dtype, uint8_t* codes,
                                     uint8_t* scales, void* stream);

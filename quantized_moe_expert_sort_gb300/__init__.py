@@ -36,7 +36,9 @@ class _SortView(ctypes.Structure):
 
 class _WorkspaceView(ctypes.Structure):
     _fields_ = [("sort", _SortView), ("act_codes", ctypes.c_void_p), ("act_scales", ctypes.c_void_p),
-                ("inter_codes", ctypes.c_void_p), ("inter_scales", ctypes.c_void_p), ("acc32", ctypes.c_void_p)]
+                ("inter_codes", ctypes.c_void_p), ("inter_scales", ctypes.c_void_p), ("acc32", ctypes.c_void_p),
+                ("act_scale_stride", ctypes.c_int32), ("inter_scale_stride", ctypes.c_int32),
+                ("inter_scale_layout", ctypes.c_int32)]
 
 
 def library_path():
@@ -203,7 +205,12 @@ class MoE:
         v = self.workspace()
         bpe = {"bf16": 2, "fp8": 1, "fp4": 0.5}[a_dtype]
         codes = _view(v.inter_codes, (rows, int(self.I * bpe)), torch.uint8).clone()
-        scales = _view(v.inter_scales, (rows, self.I // 32), torch.uint8).clone()
+        if v.inter_scale_layout == 0:
+            scales = _view(v.inter_scales, (rows, v.inter_scale_stride), torch.uint8)[:, :self.I // 32].clone()
+        else:  # 128-row tiles of 512-byte chunks (tensor-core path)
+            nb, nc = rows // 128, self.I // 128
+            raw = _view(v.inter_scales, (nb, nc, 32, 4, 4), torch.uint8)  # [tile, chunk, m%32, m/32, kb%4]
+            scales = raw.permute(0, 3, 2, 1, 4).reshape(rows, self.I // 32).clone()
         return codes, scales
 
     def set_profiling(self, enable=True):
@@ -227,8 +234,9 @@ class MoE:
 
 
 def quantize_activations(x, a_dtype, stream=None):
-    """bf16 [T,H] -> (codes, e8m0 scales [T,H/32]); codes are f16 bits [T,H] (as uint8 [T,2H]) for
-    'bf16', e4m3 [T,H] for 'fp8', e2m1 pairs [T,H/2] for 'fp4'."""
+    """bf16 [T,H] -> (codes, e8m0 scales [T,H/32]); codes are e4m3 [T,H] for 'fp8', e2m1 pairs
+    [T,H/2] for 'fp4', and for 'bf16' f16 bits [T,H] (as uint8 [T,2H]) with one scale per token
+    (repeated in all H/32 bytes of the row)."""
     _require(x, torch.bfloat16, "x")
     T, H = x.shape
     width = {"bf16": 2 * H, "fp8": H, "fp4": H // 2}[a_dtype]

@@ -29,8 +29,8 @@ void set_last_error_message(const char* msg);
 cudaError_t prep_set_smem_limits();
 cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* hist,
                         int hist_cap_chunks, int* err, cudaStream_t st);
-cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, float* acc32,
-                             int num_sms, cudaStream_t st);
+cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, int xs_stride,
+                             float* acc32, int num_sms, cudaStream_t st);
 cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t st);
 cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
@@ -44,6 +44,7 @@ struct StageParams {
   const uint8_t* wscale;
   // sort output
   const int32_t* sorted_ids;
+  const int32_t* block_expert;
   const int32_t* expert_offset;
   const int32_t* expert_count;
   const int32_t* active_experts;
@@ -53,6 +54,8 @@ struct StageParams {
   uint8_t* os;        // stage 1: [rows, I/32] scales
   float* acc32;       // stage 2: [T, H]
   const float* topk_w;  // stage 2: [T*K]
+  int xs_stride;       // bytes per row of the activation-scale array (as)
+  int os_stride;       // stage 1: bytes per row of the output-scale array (os)
   int T, H, I, E, K;
   int act;
   float beta, lbeta;
@@ -60,7 +63,18 @@ struct StageParams {
 };
 
 constexpr int DEC_TOK = 8;       // tokens per MMA column group (mma n8)
-constexpr int DEC_STAGES = 8;    // weight pipeline depth (4 KB per stage)
+
+// Row stride of the workspace's e8m0 scale arrays: kdim/32 bytes rounded up to
+// 16, so that every row can be moved with one 16-byte-aligned bulk copy.
+__host__ __device__ inline int scale_row_stride(int kdim) { return ((kdim / 32) + 15) & ~15; }
+
+// tcgen05 family (block-scaled tensor-core MMA, 128 x 128 tiles, tile_m = 128)
+enum { TC_A8W4 = 0, TC_A4W4 = 1 };
+constexpr int TC_TILE_M = 128;
+using TcParams = StageParams;
+cudaError_t tc_set_smem_limits();
+cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                            int grid, cudaStream_t st);
 
 cudaError_t decode_set_smem_limits();
 int decode_s1_blocks_per_sm(int fmt, int H);

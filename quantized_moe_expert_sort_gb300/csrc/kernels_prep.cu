@@ -219,15 +219,13 @@ __global__ void __launch_bounds__(1024) sort_place_kernel(const int32_t* __restr
 // ---------------------------------------------------------------------------
 // Activation block quantisation (S2): x bf16 [T,H] -> codes + e8m0 scales per
 // 32 along H ("Add an opt-in a4w4 SiTUv2 MoE path...", What: a8w4 = fp8,
-// a4w4 = fp4x2 activations; 1x32 scales). FMT_F16 is the a16 operand: the
-// same bf16 values re-encoded as block-scaled f16 (exact for every element no
-// more than 2^31 below its block's maximum). Also zeroes the fp32 combine
-// buffer acc32 [T,H] for the stage-2 scatter that follows.
-// One warp per (token, 32-block); lane l handles element l.
+// a4w4 = fp4x2 activations; 1x32 scales). One warp per (token, 32-block);
+// lane l handles element l. Scale rows are xs_stride bytes apart.
+// Also zeroes the fp32 combine buffer acc32 [T,H] for the stage-2 scatter.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int fmt,
                                                         uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-                                                        float* __restrict__ acc32) {
+                                                        int xs_stride, float* __restrict__ acc32) {
   int lane = threadIdx.x & 31;
   long nwarps = (long)gridDim.x * (blockDim.x >> 5);
   long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -240,7 +238,68 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
     uint32_t s;
     uint32_t code = block_quant_lane(v, fmt, &s);
     block_store_lane(xq + (t * nb + b) * bpb, code, fmt, lane);
-    if (lane == 0) xs[t * nb + b] = (uint8_t)s;
+    if (lane == 0) xs[t * xs_stride + b] = (uint8_t)s;
+  }
+  if (acc32) {
+    long n4 = (long)T * H / 4;
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
+      reinterpret_cast<float4*>(acc32)[i] = z;
+  }
+}
+
+// The bf16 activation operand: each token row re-encoded as IEEE half times
+// one power-of-two scale per row, E = floor(log2(row amax)) - 15, so that the
+// row maximum lands in [2^15, 2^16). Every bf16 value (8 significant bits) no
+// more than 2^31 below its row's maximum is represented exactly. The row scale
+// is written into every 32-block scale byte of the row, so the operand reads
+// like any other block-scaled one. One CTA per token row (H % 8 == 0), 16-byte
+// loads and stores; the remaining CTAs zero the fp32 combine buffer.
+__global__ void __launch_bounds__(256) act_encode_f16_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
+                                                             uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                                                             int xs_stride, float* __restrict__ acc32) {
+  __shared__ float red[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* row = reinterpret_cast<const uint4*>(x + t * H);
+    const int n8 = H / 8;
+    float amax = 0.0f;
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+      uint4 v = row[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
+      }
+    }
+    amax = warp_max(amax);
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    __syncthreads();
+    int E = 0;
+    uint32_t sbyte = 127;
+    if (amax > 0.0f) {
+      E = floor_log2_f32(amax) - 15;
+      E = E < -127 ? -127 : (E > 127 ? 127 : E);
+      sbyte = (uint32_t)(E + 127);
+    }
+    const float m = exp2_neg(E);
+    uint4* q = reinterpret_cast<uint4*>(xq + t * (long)H * 2);
+    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+      uint4 v = row[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float lo = __fmul_rn(__uint_as_float(w[k] << 16), m), hi = __fmul_rn(__uint_as_float(w[k] & 0xFFFF0000u), m);
+        o[k] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+      }
+      q[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    for (int b = threadIdx.x; b < H / 32; b += blockDim.x) xs[t * xs_stride + b] = (uint8_t)sbyte;
   }
   if (acc32) {
     long n4 = (long)T * H / 4;
@@ -307,14 +366,24 @@ cudaError_t prep_set_smem_limits() {
   return e;
 }
 
-cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, float* acc32, int num_sms,
-                             cudaStream_t st) {
+cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, uint8_t* xs, int xs_stride,
+                             float* acc32, int num_sms, cudaStream_t st) {
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  long cap = (long)num_sms * 8;
+  if (fmt == FMT_F16) {
+    long blocks = (long)T;
+    long zb = ((long)T * H / 4 + 255) / 256;
+    if (acc32 && zb > blocks) blocks = zb;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    act_encode_f16_kernel<<<(int)blocks, 256, 0, st>>>(xb, T, H, xq, xs, xs_stride, acc32);
+    return cudaGetLastError();
+  }
   long work = (long)T * (H / 32);
   long blocks = (work + 7) / 8;
-  long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  act_quant_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, fmt, xq, xs, acc32);
+  act_quant_kernel<<<(int)blocks, 256, 0, st>>>(xb, T, H, fmt, xq, xs, xs_stride, acc32);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,408 @@
+// Grouped stage-1 / stage-2 kernels on the 5th-generation tensor cores
+// (tcgen05 block-scaled MMA, TMEM accumulators, TMA operand staging) for many
+// routed rows per expert (prefill).
+//
+// What they compute is the same as the decode kernels ("Add Kimi-K3 A8W4
+// support..." Technical Details; "Add an opt-in a4w4 SiTUv2 MoE path...",
+// What / Performance: at large token counts the activation traffic and the MMA
+// rate matter). Kinds:
+//   a8w4: tcgen05.mma kind::mxf8f6f4, A = e4m3 activations, B = e2m1 weights
+//         (expanded by TMA to one 16-element group per 16 bytes), 1x32 e8m0
+//         scales (scale_vec::1X), K = 32 per MMA, K tile 128.
+//   a4w4: kind::mxf4, A and B packed e2m1, scale_vec::2X, K = 64 per MMA, K tile 256.
+//
+// Tile: M = 128 sorted rows (one sort block of one expert) x N = 128 weight
+// rows. Stage 1: N = 64 gate rows + the same 64 up rows, so each epilogue
+// thread (one token row) holds g and u for 64 columns j, forms y = act(g, u)
+// and requantises y per 32 along I by itself. Stage 2: N = 128 rows of H; each
+// thread adds w * z for its row into the fp32 combine buffer (vector red).
+//
+// CTA (one per SM, persistent over tiles): warp 0 issues TMA (tile::gather4 of
+// the 128 token rows for stage 1), warp 1 copies e8m0 scales into the
+// tcgen05.cp layout with cp.async, warp 2 owns TMEM and issues tcgen05.cp +
+// tcgen05.mma, warps 4-7 run the epilogue from double-buffered accumulators.
+// Scale layout in TMEM (M = 128): row m reads lane m, column base + m/32,
+// byte = the MMA's scale id; in shared memory byte 16*(m%32) + 4*(m/32) + kb
+// of a 512-byte chunk holds the scale of row m for K block kb (4 blocks).
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreadsTc = 256;
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kNS = 4;          // pipeline stages
+constexpr int kTileBytes = 128 * 128;  // one 128-row x 128-byte operand tile
+
+template <int KIND> struct Kind;
+template <> struct Kind<TC_A8W4> {
+  static constexpr int kKTile = 128;   // elements per stage
+  static constexpr int kBlocks = 4;    // 32-element scale blocks per stage
+  static constexpr int kChunks = 1;    // 512-byte scale chunks per stage and operand
+  static constexpr int kFmt = FMT_E4M3;
+};
+template <> struct Kind<TC_A4W4> {
+  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kFmt = FMT_E2M1;
+};
+
+struct TcLayout {
+  static constexpr uint32_t a = 0;                                  // kNS x 16 KB
+  static constexpr uint32_t b = a + kNS * kTileBytes;               // kNS x 16 KB
+  static constexpr uint32_t sfa = b + kNS * kTileBytes;             // kNS x 2 chunks
+  static constexpr uint32_t sfb = sfa + kNS * 1024;
+  static constexpr uint32_t bars = sfb + kNS * 1024;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4) * 8;
+  static constexpr uint32_t total = tmem_slot + 16 + 1024;        // + alignment slack
+};
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 2 * kBN;  // scale slots after the two accumulators
+
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Byte offset of (row m, block kb % 4) inside a 512-byte scale chunk.
+__device__ __forceinline__ uint32_t sf_off(int m) { return 16u * (m & 31) + 4u * (m >> 5); }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+template <int KIND, int STAGE>
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, const __grid_constant__ CUtensorMap tm_a,
+                                                                 const __grid_constant__ CUtensorMap tm_b) {
+  using KD = Kind<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);
+  uint64_t* empty = full + kNS;
+  uint64_t* tfull = empty + kNS;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcLayout::tmem_slot);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.H, I = p.I, K = p.K, T = p.T;
+  const long TK = (long)T * K;
+  const int kdim = STAGE == 1 ? H : I;
+  const int ktiles = (kdim + KD::kKTile - 1) / KD::kKTile;
+  const int nblk_k = kdim / 32;                       // valid 32-blocks along K
+  const int ntn = STAGE == 1 ? I / 64 : H / kBN;      // N tiles per expert
+  const int num_tiles = p.meta[META_NUM_BLOCKS] * ntn;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+    }
+    uint32_t stage = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int b = tile / ntn, nt = tile % ntn;
+      const int e = p.block_expert[b];
+      int rows[4];
+      if (STAGE == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int pid = p.sorted_ids[b * kBM + 4 * lane + i];
+          rows[i] = pid < TK ? pid / K : T;  // padding row: out of range -> zero fill
+        }
+      }
+      for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+        const int slot = stage % kNS;
+        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
+        uint8_t* sa = smem + TcLayout::a + slot * kTileBytes;
+        uint8_t* sb = smem + TcLayout::b + slot * kTileBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * kTileBytes);
+        __syncwarp();
+        if (STAGE == 1) {
+          tma_gather4(sa + 512 * lane, &tm_a, ks * 128, rows[0], rows[1], rows[2], rows[3], &full[slot]);
+          if (lane == 0) {
+            tma_load_4d(sb, &tm_b, ks * 128, nt * 64, 0, e, &full[slot]);
+            tma_load_4d(sb + 64 * 128, &tm_b, ks * 128, nt * 64, 1, e, &full[slot]);
+          }
+        } else if (lane == 0) {
+          tma_load_2d(sa, &tm_a, ks * 128, b * kBM, &full[slot]);
+          tma_load_3d(sb, &tm_b, ks * 128, nt * kBN, e, &full[slot]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ scale copies ------------------------------
+    uint32_t stage = 0;
+    int pending = -1;  // slot whose copies are issued but not yet signalled
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int b = tile / ntn, nt = tile % ntn;
+      const int e = p.block_expert[b];
+      const uint8_t* arow[4];
+      const uint8_t* brow[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int m = 4 * lane + i;
+        if (STAGE == 1) {
+          const int pid = p.sorted_ids[b * kBM + m];
+          arow[i] = p.as + (size_t)(pid < TK ? pid / K : 0) * p.xs_stride;
+          const int wr = m < 64 ? nt * 64 + m : I + nt * 64 + (m - 64);
+          brow[i] = p.wscale + ((size_t)e * 2 * I + wr) * (H / 32);
+        } else {
+          arow[i] = nullptr;
+          brow[i] = p.wscale + ((size_t)e * H + (size_t)nt * kBN + m) * (I / 32);
+        }
+      }
+      for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+        const int slot = stage % kNS;
+        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
+        uint8_t* dA = smem + TcLayout::sfa + slot * 1024;
+        uint8_t* dB = smem + TcLayout::sfb + slot * 1024;
+        for (int c = 0; c < KD::kChunks; ++c) {
+          const int kb0 = ks * KD::kBlocks + 4 * c;  // first 32-block of this chunk
+          const bool in = kb0 < nblk_k;              // kdim % 128 == 0: a chunk is all in or all out
+          if (STAGE == 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = 4 * lane + i;
+              if (in) cp_async4(dA + 512 * c + sf_off(m), arow[i] + kb0);
+              else *reinterpret_cast<uint32_t*>(dA + 512 * c + sf_off(m)) = 0x7F7F7F7Fu;
+            }
+          } else {
+            // intermediate scales are stored by stage 1 already in chunk layout
+            const uint8_t* src = p.as + ((size_t)b * (nblk_k / 4) + (kb0 / 4)) * 512 + 16 * lane;
+            if (in) cp_async16(dA + 512 * c + 16 * lane, src);
+            else *reinterpret_cast<uint4*>(dA + 512 * c + 16 * lane) = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int m = 4 * lane + i;
+            if (in) cp_async4(dB + 512 * c + sf_off(m), brow[i] + kb0);
+            else *reinterpret_cast<uint32_t*>(dB + 512 * c + sf_off(m)) = 0x7F7F7F7Fu;
+          }
+        }
+        cp_async_commit();
+        if (pending >= 0) {
+          cp_async_wait1();     // everything but the group just committed has landed
+          fence_proxy_async();  // generic-proxy writes -> visible to tcgen05.cp
+          mbar_arrive(&full[pending]);
+        }
+        pending = slot;
+      }
+    }
+    if (pending >= 0) {
+      cp_async_wait0();
+      fence_proxy_async();
+      mbar_arrive(&full[pending]);
+    }
+  } else if (warp == 2) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      uint32_t stage = 0;
+      int lt = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        mbar_wait_or_abort(&tempty[buf], ((lt >> 1) & 1) ^ 1, p.err, &abort_flag);
+        tc::fence_after();
+        const uint32_t d = tbase + buf * kBN;
+        for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+          const int slot = stage % kNS;
+          mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag);
+          tc::fence_after();
+          const uint32_t sfa = tbase + kSfCol0 + slot * 16;
+          const uint32_t sfb = sfa + 8;
+          for (int c = 0; c < KD::kChunks; ++c) {
+            tc::cp_32x128b_warpx4(sfa + 4 * c, tc::sdesc(smem_u32(smem + TcLayout::sfa + slot * 1024 + 512 * c), 0, 128, tc::SW_NONE));
+            tc::cp_32x128b_warpx4(sfb + 4 * c, tc::sdesc(smem_u32(smem + TcLayout::sfb + slot * 1024 + 512 * c), 0, 128, tc::SW_NONE));
+          }
+          const uint32_t sa = smem_u32(smem + TcLayout::a + slot * kTileBytes);
+          const uint32_t sb = smem_u32(smem + TcLayout::b + slot * kTileBytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint64_t da = tc::sdesc(sa + 32 * i, 16, 1024, tc::SW_128B);
+            const uint64_t db = tc::sdesc(sb + 32 * i, 16, 1024, tc::SW_128B);
+            const uint32_t acc = (ks > 0 || i > 0) ? 1u : 0u;
+            if (KIND == TC_A8W4) {
+              tc::mma_mxf8f6f4(d, da, db, tc::idesc_bs(kBM, kBN, tc::F8F6F4_E4M3, tc::F8F6F4_E2M1, i, i), sfa, sfb, acc);
+            } else {
+              const uint32_t id = tc::idesc_bs(kBM, kBN, tc::MXF4_E2M1, tc::MXF4_E2M1, 2 * (i & 1), 2 * (i & 1));
+              tc::mma_mxf4(d, da, db, id, sfa + 4 * (i >> 1), sfb + 4 * (i >> 1), acc);
+            }
+          }
+          tc::commit(&empty[slot]);
+        }
+        tc::commit(&tfull[buf]);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;
+    const int m = 32 * q + lane;           // tile row of this thread (= TMEM lane)
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      const int b = tile / ntn, nt = tile % ntn;
+      const int buf = lt & 1;
+      const int row = b * kBM + m;
+      const int pid = p.sorted_ids[row];
+      const bool valid = pid < TK;
+      mbar_wait_or_abort(&tfull[buf], (lt >> 1) & 1, p.err, &abort_flag);
+      tc::fence_after();
+      const uint32_t d = tbase + lane_off + buf * kBN;
+      if (STAGE == 1) {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t gr[32], ur[32];
+          tc::ld_32x32b_x16(d + 32 * h, gr);
+          tc::ld_32x32b_x16(d + 32 * h + 16, gr + 16);
+          tc::ld_32x32b_x16(d + 64 + 32 * h, ur);
+          tc::ld_32x32b_x16(d + 64 + 32 * h + 16, ur + 16);
+          tc::ld_wait();
+          float y[32];
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            y[i] = act_apply(p.act, __uint_as_float(gr[i]), __uint_as_float(ur[i]), p.beta, p.lbeta);
+            amax = fmaxf(amax, fabsf(y[i]));
+          }
+          if (valid) {
+            // 1x32 block quantisation of y along I (same rule as the activations)
+            const int fmt = KD::kFmt;
+            uint32_t sbyte = 127;
+            float mul = 1.0f;
+            if (amax > 0.0f) {
+              int E = floor_log2_f32(amax) - fmt_emax(fmt);
+              E = E < -127 ? -127 : (E > 127 ? 127 : E);
+              sbyte = (uint32_t)(E + 127);
+              mul = exp2_neg(E);
+            }
+            const int j0 = nt * 64 + 32 * h;  // first intermediate column of this block
+            if (fmt == FMT_E4M3) {
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t lo = amax > 0.0f ? cvt_e4m3x2(__fmul_rn(y[4 * i], mul), __fmul_rn(y[4 * i + 1], mul)) : 0u;
+                const uint32_t hi = amax > 0.0f ? cvt_e4m3x2(__fmul_rn(y[4 * i + 2], mul), __fmul_rn(y[4 * i + 3], mul)) : 0u;
+                w[i] = lo | (hi << 16);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.oq + (size_t)row * I + j0);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t acc = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint32_t byte =
+                      amax > 0.0f ? cvt_e2m1x2(__fmul_rn(y[8 * i + 2 * k], mul), __fmul_rn(y[8 * i + 2 * k + 1], mul)) : 0u;
+                  acc |= byte << (8 * k);
+                }
+                w[i] = acc;
+              }
+              *reinterpret_cast<uint4*>(p.oq + (size_t)row * (I / 2) + j0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            // scale byte in the stage-2 chunk layout
+            const int kb = j0 / 32;
+            p.os[((size_t)b * (I / 128) + kb / 4) * 512 + sf_off(m) + (kb & 3)] = (uint8_t)sbyte;
+          }
+        }
+      } else {
+        const int t = valid ? pid / K : 0;
+        const float wt = valid ? p.topk_w[pid] : 0.0f;
+        float* dst = p.acc32 + (size_t)t * H + (size_t)nt * kBN;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::ld_32x32b_x16(d + 32 * c, r);
+          tc::ld_32x32b_x16(d + 32 * c + 16, r + 16);
+          tc::ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(dst + 32 * c + 4 * i, wt * __uint_as_float(r[4 * i]), wt * __uint_as_float(r[4 * i + 1]),
+                         wt * __uint_as_float(r[4 * i + 2]), wt * __uint_as_float(r[4 * i + 3]));
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc::fence_after();
+    tc::tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int KIND, int STAGE>
+static cudaError_t set_limit_tc() {
+  return cudaFuncSetAttribute(tc_stage_kernel<KIND, STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TcLayout::total);
+}
+
+cudaError_t tc_set_smem_limits() {
+  cudaError_t e = set_limit_tc<TC_A8W4, 1>();
+  if (e == cudaSuccess) e = set_limit_tc<TC_A8W4, 2>();
+  if (e == cudaSuccess) e = set_limit_tc<TC_A4W4, 1>();
+  if (e == cudaSuccess) e = set_limit_tc<TC_A4W4, 2>();
+  return e;
+}
+
+cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                            int grid, cudaStream_t st) {
+  const size_t smem = TcLayout::total;
+  if (kind == TC_A8W4 && stage == 1) tc_stage_kernel<TC_A8W4, 1><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
+  else if (kind == TC_A8W4) tc_stage_kernel<TC_A8W4, 2><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
+  else if (stage == 1) tc_stage_kernel<TC_A4W4, 1><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
+  else tc_stage_kernel<TC_A4W4, 2><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

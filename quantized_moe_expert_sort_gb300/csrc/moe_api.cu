@@ -2,6 +2,7 @@
 // the launch sequence of the forward pass. See include/moe.h for the contract.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -79,6 +80,11 @@ struct moe_ctx {
   CUtensorMap tm_w13;
   const void* tm_w2_key;
   CUtensorMap tm_w2;
+  // tcgen05 family maps (keyed by pointer and kind)
+  const void* tm_w13tc_key; int tm_w13tc_kind; CUtensorMap tm_w13tc;
+  const void* tm_w2tc_key; int tm_w2tc_kind; CUtensorMap tm_w2tc;
+  int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
+  int last_inter_layout;
   int last_tile_m;
   // profiling (moe_set_profiling)
   int profiling;
@@ -134,6 +140,59 @@ static moe_status make_w2_map(moe_ctx* c, const uint8_t* w2) {
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(w2) failed: %d", (int)r);
   c->tm_w2_key = w2;
+  return MOE_OK;
+}
+
+static moe_status encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                         const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz, const char* what) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return MOE_OK;
+}
+
+// fp4 weights for the tcgen05 kinds: mxf8f6f4 reads e2m1 as one 16-element
+// group per 16 bytes of shared memory (TMA type 16U4_ALIGN16B expands the
+// packed rows); mxf4 reads them packed (plain bytes).
+static moe_status make_w13tc_map(moe_ctx* c, const uint8_t* w13, int kind) {
+  if (c->tm_w13tc_key == w13 && c->tm_w13tc_kind == kind) return MOE_OK;
+  const cuuint64_t H = c->H, I = c->I, E = c->E;
+  cuuint64_t strides[3] = {H / 2, I * H / 2, 2 * I * H / 2};
+  moe_status s;
+  if (kind == TC_A8W4) {
+    cuuint64_t dims[4] = {H, I, 2, E};
+    cuuint32_t box[4] = {128, 64, 1, 1};
+    s = encode(&c->tm_w13tc, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, w13, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w13 fp4 unpacked");
+  } else {
+    cuuint64_t dims[4] = {H / 2, I, 2, E};
+    cuuint32_t box[4] = {128, 64, 1, 1};
+    s = encode(&c->tm_w13tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, w13, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w13 fp4 packed");
+  }
+  if (s != MOE_OK) return s;
+  c->tm_w13tc_key = w13;
+  c->tm_w13tc_kind = kind;
+  return MOE_OK;
+}
+
+static moe_status make_w2tc_map(moe_ctx* c, const uint8_t* w2, int kind) {
+  if (c->tm_w2tc_key == w2 && c->tm_w2tc_kind == kind) return MOE_OK;
+  const cuuint64_t H = c->H, I = c->I, E = c->E;
+  cuuint64_t strides[2] = {I / 2, H * I / 2};
+  cuuint32_t box[3] = {128, 128, 1};
+  moe_status s;
+  if (kind == TC_A8W4) {
+    cuuint64_t dims[3] = {I, H, E};
+    s = encode(&c->tm_w2tc, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, w2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w2 fp4 unpacked");
+  } else {
+    cuuint64_t dims[3] = {I / 2, H, E};
+    s = encode(&c->tm_w2tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w2 fp4 packed");
+  }
+  if (s != MOE_OK) return s;
+  c->tm_w2tc_key = w2;
+  c->tm_w2tc_kind = kind;
   return MOE_OK;
 }
 
@@ -216,9 +275,9 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->meta, sizeof(int32_t) * META_WORDS},
       {(void**)&c->hist, sizeof(int32_t) * (size_t)c->hist_chunks * E},
       {(void**)&c->xq, (size_t)max_tokens * H * 2},
-      {(void**)&c->xs, (size_t)max_tokens * H / 32},
+      {(void**)&c->xs, (size_t)max_tokens * scale_row_stride(H)},
       {(void**)&c->inter_q, (size_t)c->cap_rows * I * 2},
-      {(void**)&c->inter_s, (size_t)c->cap_rows * I / 32},
+      {(void**)&c->inter_s, (size_t)c->cap_rows * scale_row_stride(I)},
       {(void**)&c->acc32, sizeof(float) * (size_t)max_tokens * H},
       {(void**)&c->err, sizeof(int) * 4},
       {(void**)&c->st_x, (size_t)max_tokens * H * 2},
@@ -238,10 +297,13 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   if (e == cudaSuccess) e = cudaMemset(c->meta, 0, sizeof(int32_t) * META_WORDS);
   if (e == cudaSuccess) e = prep_set_smem_limits();
   if (e == cudaSuccess) e = decode_set_smem_limits();
+  if (e == cudaSuccess) e = tc_set_smem_limits();
   if (e != cudaSuccess) {
     free_ctx(c);
     return cuda_fail(e, "context setup");
   }
+  c->tc_min_rows = 32;
+  if (const char* v = getenv("MOE_TC_MIN_ROWS")) c->tc_min_rows = atoi(v);
   for (int f = 0; f < 3; ++f) {
     c->s1_bps[f] = decode_s1_blocks_per_sm(f, H);
     c->s2_bps[f] = decode_s2_blocks_per_sm(f, I);
@@ -266,6 +328,9 @@ moe_status moe_get_workspace(moe_ctx* c, moe_workspace_view* v) {
   v->inter_codes = c->inter_q;
   v->inter_scales = c->inter_s;
   v->acc32 = c->acc32;
+  v->act_scale_stride = scale_row_stride(c->H);
+  v->inter_scale_stride = scale_row_stride(c->I);
+  v->inter_scale_layout = c->last_inter_layout;
   return MOE_OK;
 }
 
@@ -303,22 +368,51 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int fmt = fmt_of_adtype(adt);
   const long pairs = (long)T * c->K;
-  moe_status ms = make_w13_map(c, w13);
-  if (ms != MOE_OK) return ms;
-  ms = make_w2_map(c, w2);
-  if (ms != MOE_OK) return ms;
+  const long max_active = pairs < c->E ? pairs : c->E;
+  // Path: the tcgen05 kernels (128-row tiles of one expert) once the mean
+  // number of routed rows per active expert reaches tc_min_rows; the decode
+  // kernels (8-row groups, register-dequantised weights) below that and for
+  // bf16 activations.
+  const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active;
+  const int tile_m = use_tc ? TC_TILE_M : kDecodeTile;
+  const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
+  CUtensorMap tm_xq, tm_inter;
+  moe_status ms;
+  if (use_tc) {
+    ms = make_w13tc_map(c, w13, kind);
+    if (ms != MOE_OK) return ms;
+    ms = make_w2tc_map(c, w2, kind);
+    if (ms != MOE_OK) return ms;
+    const cuuint64_t xrow = adt == MOE_A_FP8 ? (cuuint64_t)c->H : (cuuint64_t)c->H / 2;
+    const cuuint64_t irow = adt == MOE_A_FP8 ? (cuuint64_t)c->I : (cuuint64_t)c->I / 2;
+    cuuint64_t xdims[2] = {xrow, (cuuint64_t)T}, xstr[1] = {xrow};
+    cuuint32_t xbox[2] = {128, 1};  // tile::gather4: one row per coordinate
+    ms = encode(&tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq, xdims, xstr, xbox, CU_TENSOR_MAP_SWIZZLE_128B, "activation rows");
+    if (ms != MOE_OK) return ms;
+    cuuint64_t idims[2] = {irow, (cuuint64_t)c->cap_rows}, istr[1] = {irow};
+    cuuint32_t ibox[2] = {128, 128};
+    ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate");
+    if (ms != MOE_OK) return ms;
+  } else {
+    ms = make_w13_map(c, w13);
+    if (ms != MOE_OK) return ms;
+    ms = make_w2_map(c, w2);
+    if (ms != MOE_OK) return ms;
+  }
 
   c->ev_n = 0;
   prof_mark(c, st, "sort");
-  cudaError_t e = launch_sort(ids, pairs, c->E, kDecodeTile, sort_out(c), c->hist, c->hist_chunks, c->err, st);
+  cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, sort_out(c), c->hist, c->hist_chunks, c->err, st);
   if (e != cudaSuccess) return cuda_fail(e, "sort launch");
-  c->last_tile_m = kDecodeTile;
+  c->last_tile_m = tile_m;
+  c->last_inter_layout = use_tc ? 1 : 0;
   prof_mark(c, st, "act_quant");
-  e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, c->acc32, c->num_sms, st);
+  e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
 
   StageParams p{};
   p.sorted_ids = c->sorted_ids;
+  p.block_expert = c->block_expert;
   p.expert_offset = c->expert_offset;
   p.expert_count = c->expert_count;
   p.active_experts = c->active_experts;
@@ -327,24 +421,37 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   p.act = act; p.beta = beta; p.lbeta = lbeta;
   p.err = c->err;
 
-  const long max_active = pairs < c->E ? pairs : c->E;
+  const long max_blocks = (pairs + max_active * (tile_m - 1)) / tile_m;  // upper bound on sort blocks
   StageParams p1 = p;
   p1.aq = c->xq; p1.as = c->xs; p1.wscale = w13s;
   p1.oq = c->inter_q; p1.os = c->inter_s;
-  long items1 = max_active * (c->I / 32);
-  long cap1 = (long)c->num_sms * c->s1_bps[fmt];
-  prof_mark(c, st, "stage1");
-  e = launch_decode_stage1(fmt, p1, c->tm_w13, (int)(items1 < cap1 ? items1 : cap1), st);
-  if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
-
+  p1.xs_stride = scale_row_stride(c->H);
+  p1.os_stride = scale_row_stride(c->I);
   StageParams p2 = p;
   p2.aq = c->inter_q; p2.as = c->inter_s; p2.wscale = w2s;
   p2.acc32 = c->acc32; p2.topk_w = w;
-  long items2 = max_active * (c->H / 64);
-  long cap2 = (long)c->num_sms * c->s2_bps[fmt];
-  prof_mark(c, st, "stage2");
-  e = launch_decode_stage2(fmt, p2, c->tm_w2, (int)(items2 < cap2 ? items2 : cap2), st);
-  if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
+  p2.xs_stride = scale_row_stride(c->I);
+
+  if (use_tc) {
+    long t1 = max_blocks * (c->I / 64), t2 = max_blocks * (c->H / 128);
+    prof_mark(c, st, "stage1");
+    e = launch_tc_stage(kind, 1, p1, tm_xq, c->tm_w13tc, (int)(t1 < c->num_sms ? t1 : c->num_sms), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
+    prof_mark(c, st, "stage2");
+    e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
+  } else {
+    long items1 = max_blocks * (c->I / 32);
+    long cap1 = (long)c->num_sms * c->s1_bps[fmt];
+    prof_mark(c, st, "stage1");
+    e = launch_decode_stage1(fmt, p1, c->tm_w13, (int)(items1 < cap1 ? items1 : cap1), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
+    long items2 = max_blocks * (c->H / 64);
+    long cap2 = (long)c->num_sms * c->s2_bps[fmt];
+    prof_mark(c, st, "stage2");
+    e = launch_decode_stage2(fmt, p2, c->tm_w2, (int)(items2 < cap2 ? items2 : cap2), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
+  }
 
   prof_mark(c, st, "finalize");
   e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
@@ -383,7 +490,7 @@ moe_status moe_quantize_activations(const void* x, int T, int H, int adt, uint8_
   int dev = 0, sms = 0;
   CUDA_TRY(cudaGetDevice(&dev));
   CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  cudaError_t e = launch_act_quant(x, T, H, fmt_of_adtype(adt), codes, scales, nullptr, sms,
+  cudaError_t e = launch_act_quant(x, T, H, fmt_of_adtype(adt), codes, scales, H / 32, nullptr, sms,
                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
   return MOE_OK;
