@@ -32,12 +32,35 @@ import torch
 
 from quantized_moe_expert_sort_gb300 import inputs
 
-H, I, E, K = 3584, 384, 896, 16
-SEED = 123
+CFG = inputs.CONFIGS["tp8_decode"]
+H, I, E, K = CFG.hidden, CFG.inter, CFG.experts, CFG.topk
+SEED = CFG.seed
 HEAD_T = 64
 SWEEP_T = [1, 4, 16, 64]
-PAGE_US_A16W4 = {1: 28.3, 4: 42.7, 16: 107.3, 64: 260.6}  # MI355X us1+us2 (aiter PR 4463, Performance)
+# MI355X isolated stage1+stage2 us (aiter PR 4463, Performance), TP8 shape, per activation dtype
+PAGE_US = {"bf16": {1: 28.3, 4: 42.7, 16: 107.3, 64: 260.6, 256: 374.7, 1024: 422.5, 2048: 651.3, 4096: 1087.3,
+                    8192: 1994.4, 16384: 3600.3},
+           "fp8": {1: 20.1, 4: 33.7, 16: 93.0, 64: 229.1, 256: 329.8, 1024: 365.7, 2048: 475.8, 4096: 774.4,
+                   8192: 1249.4, 16384: 2074.8},
+           "fp4": {1: 20.0, 4: 32.9, 16: 91.2, 64: 225.9, 256: 325.3, 1024: 349.9, 2048: 428.2, 4096: 653.2,
+                   8192: 1020.3, 16384: 1716.5}}
 L2_FLUSH_BYTES = 256 << 20
+
+
+def select_config(name):
+    """Point the module-level workload constants at one of the named configs."""
+    global CFG, H, I, E, K, SEED, SWEEP_T, HEAD_T
+    CFG = inputs.CONFIGS[name]
+    H, I, E, K, SEED = CFG.hidden, CFG.inter, CFG.experts, CFG.topk, CFG.seed
+    SWEEP_T = list(CFG.tokens)
+    HEAD_T = 64 if name == "tp8_decode" else CFG.tokens[-1]
+
+
+def workload_text(T):
+    c = CFG
+    act = "SiTUv2 beta 4 / linear beta 25" if "situv2" in c.acts else "SiLU"
+    return ("%s: hidden %d, inter %d, %d experts, top-%d %s routing, %s, a_dtype %s, bf16 out, seed %d, T=%d"
+            % (c.notes, c.hidden, c.inter, c.experts, c.topk, c.routing, act, c.a_dtype, c.seed, T))
 
 
 def log(*a):
@@ -136,10 +159,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def device_weights(device, seed=SEED, chunk=32):
+def device_weights(device, seed=None, chunk=32):
     """MXFP4 weights of all experts, drawn on the device (seeded per expert) and
     quantised by the library's own GPU quantiser."""
     import quantized_moe_expert_sort_gb300 as moe
+    seed = SEED if seed is None else seed
     w13 = torch.empty((E, 2 * I, H // 2), dtype=torch.uint8, device=device)
     w13s = torch.empty((E, 2 * I, H // 32), dtype=torch.uint8, device=device)
     w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
@@ -153,19 +177,22 @@ def device_weights(device, seed=SEED, chunk=32):
     return w13, w13s, w2, w2s
 
 
-def batch(T, device, seed=SEED):
+def batch(T, device, seed=None):
+    seed = SEED if seed is None else seed
     x = inputs.make_x(T, H, seed)
-    ids, w = inputs.make_routing(T, E, K, "uniform", seed)
+    ids, w = inputs.make_routing(T, E, K, CFG.routing, seed, CFG.zipf_s)
     return x, ids, w, x.to(device), ids.to(device), w.to(device)
 
 
-def algo_bytes(T, n_active, n_pairs, a_bytes=2):
+def algo_bytes(T, n_active, n_pairs, a_bytes=None):
     """Algorithmic bytes: active experts' weights (fp4 + e8m0), x once, the
     intermediate written and read once, out once (bf16)."""
+    if a_bytes is None:
+        a_bytes = {"bf16": 2.0, "fp8": 1.0 + 1 / 32, "fp4": 0.5 + 1 / 32}[CFG.a_dtype]
     w13 = n_active * 2 * I * (H // 2 + H // 32)
     w2 = n_active * H * (I // 2 + I // 32)
     x = T * H * 2
-    inter = n_pairs * I * a_bytes
+    inter = int(n_pairs * I * a_bytes)
     out = T * H * 2
     return dict(stage1=w13 + x + inter, stage2=w2 + inter + out, call=w13 + w2 + x + 2 * inter + out)
 
@@ -205,13 +232,15 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(device)
     t_setup = time.time()
     w13, w13s, w2, w2s = device_weights(device)
-    ctx = moe.MoE(H, I, E, K, max(SWEEP_T + [args.tokens]), device=local)
+    ctx = moe.MoE(H, I, E, K, max(SWEEP_T + [args.tokens]) if not args.no_sweep else args.tokens, device=local)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     log("setup %.1fs" % (time.time() - t_setup))
 
+    ACT = args.act or CFG.acts[-1]
+
     def fwd(xd, idd, wd, out):
-        ctx.forward(xd, idd, wd, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out)
+        ctx.forward(xd, idd, wd, w13, w13s, w2, w2s, ACT, 4.0, 25.0, CFG.a_dtype, out=out)
 
     def timed_loop(T, steps, warmup):
         x, ids, w, xd, idd, wd = batch(T, device)
@@ -277,6 +306,7 @@ def run_ours(args, world, rank, local, pg):
                 per.setdefault(name, []).append(t)
     ctx.set_profiling(False)
     per_avg = {k: statistics.mean(v) for k, v in per.items()}
+    tile_m = ctx.last_sort()["tile_m"]
     srt = ctx.last_sort()
     n_active = srt["num_active"]
     n_pairs = int((srt["sorted_ids"] < args.tokens * K).sum().item())
@@ -284,11 +314,12 @@ def run_ours(args, world, rank, local, pg):
     dominant = max(("stage1", "stage2"), key=lambda k: per_avg.get(k, 0.0))
     peak, peak_kind = measured_peaks()
     achieved = ab[dominant] / (per_avg[dominant] * 1e-3) / 1e9
+    flops = 6.0 * n_pairs * H * I
     traffic = stored_traffic(dominant, args.tokens)
 
     # --- sweep over the decode token tiers
     sweep = {}
-    for T in SWEEP_T:
+    for T in ([] if args.no_sweep else SWEEP_T):
         ms_t, _ = timed_loop(T, max(10, args.steps // 2), 3)
         sweep[str(T)] = round(statistics.mean(ms_t) * 1000.0, 2)
 
@@ -298,13 +329,13 @@ def run_ours(args, world, rank, local, pg):
     w_h = w.pin_memory()
     out_h = torch.empty((args.tokens, H), dtype=torch.bfloat16).pin_memory()
     for _ in range(args.warmup):
-        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out_h)
+        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, ACT, 4.0, 25.0, CFG.a_dtype, out=out_h)
     e2e = []
     for _ in range(args.steps):
         flush.zero_()
         torch.cuda.synchronize(device)
         ts = time.perf_counter()
-        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", out=out_h)
+        ctx.forward_host(x_h, ids_h, w_h, w13, w13s, w2, w2s, ACT, 4.0, 25.0, CFG.a_dtype, out=out_h)
         e2e.append((time.perf_counter() - ts) * 1e6)
     e2e_us = max_over_ranks(pg, statistics.mean(e2e), device) / world
     st, flags = ctx.get_error()
@@ -321,12 +352,15 @@ def run_ours(args, world, rank, local, pg):
         "ms_per_step": round(step_ms_max, 5),
         "higher_is_better": False,
         "scaling": "weak",
-        "vs_baseline": round(value_us / PAGE_US_A16W4[args.tokens], 4) if args.tokens in PAGE_US_A16W4 else None,
-        "dtype": "e2m1 x bf16 (re-encoded f16), fp32 accumulate",
+        "vs_baseline": (round(value_us / PAGE_US[CFG.a_dtype][args.tokens], 4)
+                        if (I == 384 and E == 896 and args.tokens in PAGE_US[CFG.a_dtype]) else None),
+        "dtype": {"bf16": "e2m1 x bf16 (re-encoded f16), fp32 accumulate",
+                  "fp8": "e2m1 x e4m3 block-scaled (1x32 e8m0), fp32 accumulate",
+                  "fp4": "e2m1 x e2m1 block-scaled (1x32 e8m0), fp32 accumulate"}[CFG.a_dtype],
         "data": "synthetic (seeded; weights drawn on the GPU and MXFP4-quantised by the library)",
-        "config": {"workload": "Kimi-K3 TP8-shard decode a16w4: hidden 3584, inter 384, 896 experts, top-16 uniform, "
-                               "SiTUv2 beta 4 / linear beta 25, bf16 out, seed 123",
-                   "tokens": args.tokens, "a_dtype": "bf16", "act": "situv2",
+        "config": {"workload": workload_text(args.tokens), "name": args.config,
+                   "tokens": args.tokens, "a_dtype": CFG.a_dtype, "act": ACT, "path_tile_m": tile_m,
+                   "tflops": round(flops / (step_ms * 1e-3) / 1e12, 2),
                    "l2": "flushed before every timed step (256 MB memset, outside the events)",
                    "active_experts": n_active, "routed_pairs": n_pairs,
                    "sweep_us_per_call": sweep, "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -352,7 +386,7 @@ def run_ours(args, world, rank, local, pg):
 def _oracle_inputs(T, sample):
     import oracle
     x = inputs.make_x(T, H, SEED)
-    ids, w = inputs.make_routing(T, E, K, "uniform", SEED)
+    ids, w = inputs.make_routing(T, E, K, CFG.routing, SEED, CFG.zipf_s)
     sub = np.arange(min(sample, T), dtype=np.int32)
     experts = np.unique(ids.numpy()[sub])
     w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
@@ -370,7 +404,7 @@ def _oracle_step(args_in):
     import oracle
     xb, ids, w, w13, w13s, w2, w2s, sub = args_in
     t = time.perf_counter()
-    oracle.moe_forward(xb, ids, w, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "bf16", subset=sub)
+    oracle.moe_forward(xb, ids, w, w13, w13s, w2, w2s, CFG.acts[-1], 4.0, 25.0, CFG.a_dtype, subset=sub)
     return time.perf_counter() - t
 
 
@@ -402,8 +436,7 @@ def run_reference(args, world, rank, local, pg):
         "value": round(us, 1), "unit": "us/call", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; weights quantised by the oracle)",
-        "config": {"workload": "Kimi-K3 TP8-shard decode a16w4: hidden 3584, inter 384, 896 experts, top-16 uniform, "
-                               "SiTUv2 beta 4 / linear beta 25, bf16 out, seed 123", "tokens": args.tokens},
+        "config": {"workload": workload_text(args.tokens), "name": args.config, "tokens": args.tokens},
         "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -416,7 +449,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--tokens", type=int, default=HEAD_T)
+    ap.add_argument("--config", default="tp8_decode", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--act", default=None, choices=["silu", "situv2"])
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps around the timed region")
     ap.add_argument("--cpu-sample", type=int, default=16)
     ap.add_argument("--ref-sample", type=int, default=4)
@@ -424,6 +460,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    select_config(args.config)
+    if args.tokens is None:
+        args.tokens = HEAD_T
     world, rank, local, pg = dist_setup()
     if args.impl == "reference":
         res = run_reference(args, world, rank, local, pg)

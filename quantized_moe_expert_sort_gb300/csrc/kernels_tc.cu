@@ -17,10 +17,13 @@
 // and requantises y per 32 along I by itself. Stage 2: N = 128 rows of H; each
 // thread adds w * z for its row into the fp32 combine buffer (vector red).
 //
-// CTA (one per SM, persistent over tiles): warp 0 issues TMA (tile::gather4 of
-// the 128 token rows for stage 1), warp 1 copies e8m0 scales into the
-// tcgen05.cp layout with cp.async, warp 2 owns TMEM and issues tcgen05.cp +
-// tcgen05.mma, warps 4-7 run the epilogue from double-buffered accumulators.
+// CTA (one per SM, persistent over tiles): warp 0 issues the weight TMA loads
+// and, for stage 1, gathers the 128 token rows with cp.async straight into the
+// 128B-swizzled K-major layout (stage 2 reads its contiguous rows by TMA);
+// warp 1 copies e8m0 scales into the tcgen05.cp layout with cp.async; warp 2
+// owns TMEM and issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue
+// from double-buffered accumulators. cp.async writes are made visible to the
+// tensor core by wait_group -> fence.proxy.async -> mbarrier arrive.
 // Scale layout in TMEM (M = 128): row m reads lane m, column base + m/32,
 // byte = the MMA's scale id; in shared memory byte 16*(m%32) + 4*(m/32) + kb
 // of a 512-byte chunk holds the scale of row m for K block kb (4 blocks).
@@ -48,6 +51,12 @@ template <> struct Kind<TC_A4W4> {
   static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kFmt = FMT_E2M1;
 };
 
+// Transaction bytes a weight tile reports to its mbarrier: TMA counts the packed
+// global bytes, also for the 16U4_ALIGN16B type that expands each 8-byte group
+// of 16 fp4 codes into 16 bytes of shared memory (the 8-byte gaps are left as
+// they are, so the B tiles are zeroed once at kernel start).
+template <int KIND> constexpr uint32_t weight_tile_tx() { return KIND == TC_A8W4 ? kTileBytes / 2 : kTileBytes; }
+
 struct TcLayout {
   static constexpr uint32_t a = 0;                                  // kNS x 16 KB
   static constexpr uint32_t b = a + kNS * kTileBytes;               // kNS x 16 KB
@@ -60,15 +69,6 @@ struct TcLayout {
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 2 * kBN;  // scale slots after the two accumulators
-
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcLayout::tmem_slot);
   __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t drain;  // completion of every tcgen05 op of the MMA thread
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, I = p.I, K = p.K, T = p.T;
@@ -122,9 +123,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+    // full: the TMA issuer's expect_tx arrive + 32 scale-copy lanes (+ 32 row-gather lanes in stage 1)
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], STAGE == 1 ? 1 + 32 + 32 : 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    mbar_init(&drain, 1);
     fence_barrier_init();
+  }
+  if (KIND == TC_A8W4) {
+    // zero the weight tiles: the unpacking TMA never writes their 8-byte gaps
+    for (uint32_t i = threadIdx.x; i < kNS * kTileBytes / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(smem + TcLayout::b)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
   }
   if (warp == 2) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -136,21 +145,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
+    // -------------------- operand producer (TMA + row gather) --------------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
     }
+    const size_t xrow = KIND == TC_A8W4 ? (size_t)H : (size_t)H / 2;  // bytes per activation row
     uint32_t stage = 0;
+    int pending = -1;  // stage-1 slot whose row copies are issued but not yet signalled
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int b = tile / ntn, nt = tile % ntn;
       const int e = p.block_expert[b];
-      int rows[4];
+      const uint8_t* src_row[4];
       if (STAGE == 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int pid = p.sorted_ids[b * kBM + 4 * lane + i];
-          rows[i] = pid < TK ? pid / K : T;  // padding row: out of range -> zero fill
+          // padding rows copy token 0: finite data whose output rows are never stored
+          src_row[i] = p.aq + (size_t)(pid < TK ? pid / K : 0) * xrow;
         }
       }
       for (int ks = 0; ks < ktiles; ++ks, ++stage) {
@@ -158,19 +170,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
         uint8_t* sa = smem + TcLayout::a + slot * kTileBytes;
         uint8_t* sb = smem + TcLayout::b + slot * kTileBytes;
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * kTileBytes);
-        __syncwarp();
         if (STAGE == 1) {
-          tma_gather4(sa + 512 * lane, &tm_a, ks * 128, rows[0], rows[1], rows[2], rows[3], &full[slot]);
           if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], weight_tile_tx<KIND>());
             tma_load_4d(sb, &tm_b, ks * 128, nt * 64, 0, e, &full[slot]);
             tma_load_4d(sb + 64 * 128, &tm_b, ks * 128, nt * 64, 1, e, &full[slot]);
           }
+          // 128 token rows x 128 bytes, written in the 128B-swizzled K-major layout
+          const int kbyte = ks * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 4 * lane + i;
+            const bool in = kbyte < (int)xrow;  // the last K tile of a partial row stays zero-padded below
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint8_t* dst = sa + r * 128 + (((j ^ (r & 7)) & 7) << 4);
+              if (in && kbyte + 16 * j < (int)xrow) cp_async16(dst, src_row[i] + kbyte + 16 * j);
+              else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          cp_async_commit();
+          if (pending >= 0) {
+            cp_async_wait1();
+            fence_proxy_async();
+            mbar_arrive(&full[pending]);
+          }
+          pending = slot;
         } else if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], kTileBytes + weight_tile_tx<KIND>());
           tma_load_2d(sa, &tm_a, ks * 128, b * kBM, &full[slot]);
           tma_load_3d(sb, &tm_b, ks * 128, nt * kBN, e, &full[slot]);
         }
       }
+    }
+    if (STAGE == 1 && pending >= 0) {
+      cp_async_wait0();
+      fence_proxy_async();
+      mbar_arrive(&full[pending]);
     }
   } else if (warp == 1) {
     // ------------------------------ scale copies ------------------------------
@@ -274,6 +310,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         }
         tc::commit(&tfull[buf]);
       }
+      // every MMA / copy this thread issued has finished before TMEM is released
+      tc::commit(&drain);
+      mbar_wait(&drain, 0, p.err);
     }
   } else if (warp >= 4) {
     // ------------------------------ epilogue ------------------------------
@@ -288,6 +327,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
       const int pid = p.sorted_ids[row];
       const bool valid = pid < TK;
       mbar_wait_or_abort(&tfull[buf], (lt >> 1) & 1, p.err, &abort_flag);
+      __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
       tc::fence_after();
       const uint32_t d = tbase + lane_off + buf * kBN;
       if (STAGE == 1) {
@@ -375,6 +415,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   tc::fence_before();
   __syncthreads();
   if (warp == 2) {
+    __syncwarp();
     tc::fence_after();
     tc::tmem_dealloc(tbase, kTmemCols);
   }

@@ -376,19 +376,14 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active;
   const int tile_m = use_tc ? TC_TILE_M : kDecodeTile;
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
-  CUtensorMap tm_xq, tm_inter;
+  CUtensorMap tm_inter;
   moe_status ms;
   if (use_tc) {
     ms = make_w13tc_map(c, w13, kind);
     if (ms != MOE_OK) return ms;
     ms = make_w2tc_map(c, w2, kind);
     if (ms != MOE_OK) return ms;
-    const cuuint64_t xrow = adt == MOE_A_FP8 ? (cuuint64_t)c->H : (cuuint64_t)c->H / 2;
     const cuuint64_t irow = adt == MOE_A_FP8 ? (cuuint64_t)c->I : (cuuint64_t)c->I / 2;
-    cuuint64_t xdims[2] = {xrow, (cuuint64_t)T}, xstr[1] = {xrow};
-    cuuint32_t xbox[2] = {128, 1};  // tile::gather4: one row per coordinate
-    ms = encode(&tm_xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq, xdims, xstr, xbox, CU_TENSOR_MAP_SWIZZLE_128B, "activation rows");
-    if (ms != MOE_OK) return ms;
     cuuint64_t idims[2] = {irow, (cuuint64_t)c->cap_rows}, istr[1] = {irow};
     cuuint32_t ibox[2] = {128, 128};
     ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate");
@@ -435,7 +430,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   if (use_tc) {
     long t1 = max_blocks * (c->I / 64), t2 = max_blocks * (c->H / 128);
     prof_mark(c, st, "stage1");
-    e = launch_tc_stage(kind, 1, p1, tm_xq, c->tm_w13tc, (int)(t1 < c->num_sms ? t1 : c->num_sms), st);
+    e = launch_tc_stage(kind, 1, p1, tm_inter /* unused by stage 1 */, c->tm_w13tc, (int)(t1 < c->num_sms ? t1 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     prof_mark(c, st, "stage2");
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
