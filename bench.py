@@ -269,8 +269,8 @@ def run_ours(args, world, rank, local, pg):
     time.sleep(0.5)
     t_soak = time.time()
     soak_until = t_soak + args.soak
-    xs_, ids_, ws_, xd_, idd_, wd_ = batch(HEAD_T, device)
-    out_soak = torch.empty((HEAD_T, H), dtype=torch.bfloat16, device=device)
+    xs_, ids_, ws_, xd_, idd_, wd_ = batch(args.tokens, device)
+    out_soak = torch.empty((args.tokens, H), dtype=torch.bfloat16, device=device)
     while time.time() < soak_until:
         for _ in range(20):
             fwd(xd_, idd_, wd_, out_soak)

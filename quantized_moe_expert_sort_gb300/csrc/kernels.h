@@ -17,6 +17,7 @@ struct SortOut {
   int32_t* expert_offset;   // [E+1]        first sorted row of each expert (padded prefix sum)
   int32_t* active_experts;  // [E]          experts with count > 0, ascending
   int32_t* meta;            // [META_WORDS] num_blocks, num_active, num_rows
+  int32_t* pair_row = nullptr;  // [T*K] (optional) sorted row of each pair, -1 if dropped
 };
 
 constexpr int SORT_SMALL_MAX_PAIRS = 8192;  // single-CTA sort up to this many pairs
@@ -34,6 +35,12 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
 cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t st);
 cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
+// Activation quantisation written straight into sorted order (tensor-core path):
+// codes of pair p's row go to row pair_row[p] of xq_sorted (row_bytes apart),
+// its e8m0 scales into 512-byte tcgen05.cp chunks per 128-row tile.
+cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
+                                    uint8_t* xq_sorted, uint8_t* xs_chunks, float* acc32, int num_sms,
+                                    cudaStream_t st);
 
 // Parameters of the grouped stage kernels (decode family).
 struct StageParams {
@@ -71,6 +78,7 @@ __host__ __device__ inline int scale_row_stride(int kdim) { return ((kdim / 32) 
 // tcgen05 family (block-scaled tensor-core MMA, 128 x 128 tiles, tile_m = 128)
 enum { TC_A8W4 = 0, TC_A4W4 = 1 };
 constexpr int TC_TILE_M = 128;
+constexpr int TC_MAX_K = 4096;  // reduction length the tensor-core stages accept (weight-scale staging)
 using TcParams = StageParams;
 cudaError_t tc_set_smem_limits();
 cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b,

@@ -93,7 +93,7 @@ __device__ void sort_scan_and_fill(const int* cnt, int* cursor, int E, int tile_
 // pair among equal experts is (pairs of earlier warps, from a per-expert byte
 // table) + (earlier lanes of its warp, from __match_any_sync).
 __device__ void sort_place_range(const int32_t* ids, long p0, long p1, int E, int* cursor,
-                                 uint8_t* wtab /* [E][32] */, int32_t* sorted_ids) {
+                                 uint8_t* wtab /* [E][32] */, int32_t* sorted_ids, int32_t* pair_row) {
   int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned lt_mask = (1u << lane) - 1u;
   for (long base = p0; base < p1; base += blockDim.x) {
@@ -123,7 +123,11 @@ __device__ void sort_place_range(const int32_t* ids, long p0, long p1, int E, in
           prefix += __dp4a((int)(word & keep), 0x01010101, 0);
         }
       }
-      sorted_ids[cursor[e] + prefix + rank] = (int32_t)p;
+      const int pos = cursor[e] + prefix + rank;
+      sorted_ids[pos] = (int32_t)p;
+      if (pair_row) pair_row[p] = pos;
+    } else if (pair_row && p < p1) {
+      pair_row[p] = -1;
     }
     __syncthreads();
     if (e >= 0 && leader) {
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t* __restr
   __syncthreads();
   sort_scan_and_fill(cnt, cursor, E, tile_m, n, so, scan_smem);
   __syncthreads();
-  sort_place_range(ids, 0, n, E, cursor, wtab, so.sorted_ids);
+  sort_place_range(ids, 0, n, E, cursor, wtab, so.sorted_ids, so.pair_row);
 }
 
 // Multi-CTA sort, pass 1: per-chunk histograms hist[g][e].
@@ -205,7 +209,8 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int* __restrict__ hist,
 
 // Multi-CTA sort, pass 3: stable placement of each chunk.
 __global__ void __launch_bounds__(1024) sort_place_kernel(const int32_t* __restrict__ ids, long n, int E, int chunk,
-                                                          const int* __restrict__ hist, int32_t* sorted_ids) {
+                                                          const int* __restrict__ hist, int32_t* sorted_ids,
+                                                          int32_t* pair_row) {
   extern __shared__ __align__(16) uint8_t smem[];
   int* cursor = reinterpret_cast<int*>(smem);
   uint8_t* wtab = reinterpret_cast<uint8_t*>(cursor + E);
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(1024) sort_place_kernel(const int32_t* __restr
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(wtab)[i] = 0u;
   __syncthreads();
   long p0 = (long)blockIdx.x * chunk, p1 = min(n, p0 + chunk);
-  sort_place_range(ids, p0, p1, E, cursor, wtab, sorted_ids);
+  sort_place_range(ids, p0, p1, E, cursor, wtab, sorted_ids, pair_row);
 }
 
 // ---------------------------------------------------------------------------
@@ -309,6 +314,44 @@ __global__ void __launch_bounds__(256) act_encode_f16_kernel(const __nv_bfloat16
   }
 }
 
+// Activation quantisation into sorted order for the tensor-core path: one warp
+// per (token, 32-block); the block's codes are written to the sorted row of
+// every routed pair of the token, its scale byte into the tile's 512-byte
+// chunk (byte 16*(m%32) + 4*(m/32) + b%4 of chunk b/4, m = row % 128).
+__global__ void __launch_bounds__(256) act_quant_sorted_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+                                                               int fmt, const int32_t* __restrict__ pair_row,
+                                                               uint8_t* __restrict__ xq_sorted,
+                                                               uint8_t* __restrict__ xs_chunks,
+                                                               float* __restrict__ acc32) {
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nb = H / 32;
+  const int bpb = fmt_bytes_per_32(fmt);
+  const size_t row_bytes = (size_t)nb * bpb;
+  for (long blk = gw; blk < (long)T * nb; blk += nwarps) {
+    const long t = blk / nb;
+    const int b = (int)(blk % nb);
+    const float v = __bfloat162float(x[t * H + b * 32 + lane]);
+    uint32_t s;
+    const uint32_t code = block_quant_lane(v, fmt, &s);
+    for (int k = 0; k < K; ++k) {
+      const int r = pair_row[t * K + k];
+      if (r < 0) continue;  // dropped pair (warp-uniform)
+      block_store_lane(xq_sorted + (size_t)r * row_bytes + (size_t)b * bpb, code, fmt, lane);
+      if (lane == 0)
+        xs_chunks[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (b & 3)] =
+            (uint8_t)s;
+    }
+  }
+  if (acc32) {
+    long n4 = (long)T * H / 4;
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
+      reinterpret_cast<float4*>(acc32)[i] = z;
+  }
+}
+
 // MXFP4 weight quantisation: fp32 [rows, cols] -> e2m1 codes [rows, cols/2] +
 // e8m0 scales [rows, cols/32], the same 1x32 rule as the activations.
 __global__ void __launch_bounds__(256) weight_quant_kernel(const float* __restrict__ w, long nblocks,
@@ -353,7 +396,8 @@ cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const Sor
   if (G > hist_cap_chunks) return cudaErrorInvalidValue;
   sort_hist_kernel<<<G, 1024, (size_t)E * 4, st>>>(ids, n, E, chunk, hist, err);
   sort_scan_kernel<<<1, 1024, (size_t)E * 8 + 32 * 4, st>>>(hist, G, E, tile_m, (int)n, so);
-  sort_place_kernel<<<G, 1024, (size_t)E * 4 + (size_t)E * 32, st>>>(ids, n, E, chunk, hist, so.sorted_ids);
+  sort_place_kernel<<<G, 1024, (size_t)E * 4 + (size_t)E * 32, st>>>(ids, n, E, chunk, hist, so.sorted_ids,
+                                                                     so.pair_row);
   return cudaGetLastError();
 }
 
@@ -384,6 +428,19 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   act_quant_kernel<<<(int)blocks, 256, 0, st>>>(xb, T, H, fmt, xq, xs, xs_stride, acc32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
+                                    uint8_t* xq_sorted, uint8_t* xs_chunks, float* acc32, int num_sms,
+                                    cudaStream_t st) {
+  long work = (long)T * (H / 32);
+  long blocks = (work + 7) / 8;
+  long cap = (long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  act_quant_sorted_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, fmt,
+                                                       pair_row, xq_sorted, xs_chunks, acc32);
   return cudaGetLastError();
 }
 

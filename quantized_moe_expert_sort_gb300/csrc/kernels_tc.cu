@@ -17,13 +17,15 @@
 // and requantises y per 32 along I by itself. Stage 2: N = 128 rows of H; each
 // thread adds w * z for its row into the fp32 combine buffer (vector red).
 //
-// CTA (one per SM, persistent over tiles): warp 0 issues the weight TMA loads
-// and, for stage 1, gathers the 128 token rows with cp.async straight into the
-// 128B-swizzled K-major layout (stage 2 reads its contiguous rows by TMA);
-// warp 1 copies e8m0 scales into the tcgen05.cp layout with cp.async; warp 2
-// owns TMEM and issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue
-// from double-buffered accumulators. cp.async writes are made visible to the
-// tensor core by wait_group -> fence.proxy.async -> mbarrier arrive.
+// CTA (one per SM, persistent over tiles): warp 0 issues all loads with TMA /
+// bulk copies -- the 128 sorted rows (stage 1 reads activations the quantiser
+// wrote in sorted order, stage 2 the intermediate), the weight tile, the rows'
+// e8m0 scales (already in tcgen05.cp chunks in global memory) per stage, and the
+// tile's weight scales (row-major) once per tile into a staging buffer; warp 1
+// transposes the stage's weight scales from staging into the tcgen05.cp chunk
+// layout (smem to smem, fence.proxy.async, mbarrier arrive); warp 2 owns TMEM
+// and issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue from
+// double-buffered accumulators.
 // Scale layout in TMEM (M = 128): row m reads lane m, column base + m/32,
 // byte = the MMA's scale id; in shared memory byte 16*(m%32) + 4*(m/32) + kb
 // of a 512-byte chunk holds the scale of row m for K block kb (4 blocks).
@@ -62,8 +64,10 @@ struct TcLayout {
   static constexpr uint32_t b = a + kNS * kTileBytes;               // kNS x 16 KB
   static constexpr uint32_t sfa = b + kNS * kTileBytes;             // kNS x 2 chunks
   static constexpr uint32_t sfb = sfa + kNS * 1024;
-  static constexpr uint32_t bars = sfb + kNS * 1024;
-  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4) * 8;
+  static constexpr uint32_t ws = sfb + kNS * 1024;                 // 2 x weight-scale staging
+  static constexpr uint32_t ws_bytes = 128 * 128;                  // 128 rows x up to 128 scale bytes (K <= 4096)
+  static constexpr uint32_t bars = ws + 2 * ws_bytes;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 8) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;        // + alignment slack
 };
 
@@ -78,15 +82,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
@@ -108,6 +103,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   uint64_t* empty = full + kNS;
   uint64_t* tfull = empty + kNS;
   uint64_t* tempty = tfull + 2;
+  uint64_t* wsfull = tempty + 2;   // weight scales of a tile landed in staging
+  uint64_t* wsempty = wsfull + 2;  // staging buffer free again
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TcLayout::tmem_slot);
   __shared__ int abort_flag;
   __shared__ __align__(8) uint64_t drain;  // completion of every tcgen05 op of the MMA thread
@@ -123,9 +120,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // full: the TMA issuer's expect_tx arrive + 32 scale-copy lanes (+ 32 row-gather lanes in stage 1)
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], STAGE == 1 ? 1 + 32 + 32 : 1 + 32); mbar_init(&empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 4); }
+    // full: the TMA issuer's expect_tx arrive + the 32 scale-copy lanes
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], 4);
+      mbar_init(&wsfull[s], 1);
+      mbar_init(&wsempty[s], 32);
+    }
     mbar_init(&drain, 1);
     fence_barrier_init();
   }
@@ -145,91 +147,60 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0) {
-    // -------------------- operand producer (TMA + row gather) --------------------
+    // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
-    }
-    const size_t xrow = KIND == TC_A8W4 ? (size_t)H : (size_t)H / 2;  // bytes per activation row
-    uint32_t stage = 0;
-    int pending = -1;  // stage-1 slot whose row copies are issued but not yet signalled
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int b = tile / ntn, nt = tile % ntn;
-      const int e = p.block_expert[b];
-      const uint8_t* src_row[4];
-      if (STAGE == 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int pid = p.sorted_ids[b * kBM + 4 * lane + i];
-          // padding rows copy token 0: finite data whose output rows are never stored
-          src_row[i] = p.aq + (size_t)(pid < TK ? pid / K : 0) * xrow;
-        }
-      }
-      for (int ks = 0; ks < ktiles; ++ks, ++stage) {
-        const int slot = stage % kNS;
-        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
-        uint8_t* sa = smem + TcLayout::a + slot * kTileBytes;
-        uint8_t* sb = smem + TcLayout::b + slot * kTileBytes;
+      const int sb_row = kdim / 32;  // weight-scale bytes per row
+      uint32_t stage = 0;
+      int lt = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+        const int b = tile / ntn, nt = tile % ntn;
+        const int e = p.block_expert[b];
+        // the tile's weight scales, row-major, into the staging buffer of this tile parity
+        const int tp = lt & 1;
+        if (!mbar_wait_or_abort(&wsempty[tp], ((lt >> 1) & 1) ^ 1, p.err, &abort_flag)) break;
+        uint8_t* wst = smem + TcLayout::ws + tp * TcLayout::ws_bytes;
+        mbar_arrive_expect_tx(&wsfull[tp], 128u * sb_row);
         if (STAGE == 1) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full[slot], weight_tile_tx<KIND>());
+          const uint8_t* g = p.wscale + ((size_t)e * 2 * I + (size_t)nt * 64) * sb_row;
+          bulk_g2s(wst, g, 64u * sb_row, &wsfull[tp]);
+          bulk_g2s(wst + 64 * sb_row, g + (size_t)I * sb_row, 64u * sb_row, &wsfull[tp]);
+        } else {
+          bulk_g2s(wst, p.wscale + ((size_t)e * H + (size_t)nt * kBN) * sb_row, 128u * sb_row, &wsfull[tp]);
+        }
+        for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+          const int slot = stage % kNS;
+          if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
+          uint8_t* sa = smem + TcLayout::a + slot * kTileBytes;
+          uint8_t* sb = smem + TcLayout::b + slot * kTileBytes;
+          int nchunk = 0;  // row-scale chunks of this stage inside K (the rest are filled by the scale warp)
+          for (int c = 0; c < KD::kChunks; ++c) nchunk += (ks * KD::kBlocks + 4 * c) < nblk_k;
+          mbar_arrive_expect_tx(&full[slot], kTileBytes + weight_tile_tx<KIND>() + 512u * nchunk);
+          // A: 128 sorted rows (stage 1: activations written in sorted order; stage 2: the intermediate)
+          tma_load_2d(sa, &tm_a, ks * 128, b * kBM, &full[slot]);
+          if (STAGE == 1) {
             tma_load_4d(sb, &tm_b, ks * 128, nt * 64, 0, e, &full[slot]);
             tma_load_4d(sb + 64 * 128, &tm_b, ks * 128, nt * 64, 1, e, &full[slot]);
+          } else {
+            tma_load_3d(sb, &tm_b, ks * 128, nt * kBN, e, &full[slot]);
           }
-          // 128 token rows x 128 bytes, written in the 128B-swizzled K-major layout
-          const int kbyte = ks * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = 4 * lane + i;
-            const bool in = kbyte < (int)xrow;  // the last K tile of a partial row stays zero-padded below
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint8_t* dst = sa + r * 128 + (((j ^ (r & 7)) & 7) << 4);
-              if (in && kbyte + 16 * j < (int)xrow) cp_async16(dst, src_row[i] + kbyte + 16 * j);
-              else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-          cp_async_commit();
-          if (pending >= 0) {
-            cp_async_wait1();
-            fence_proxy_async();
-            mbar_arrive(&full[pending]);
-          }
-          pending = slot;
-        } else if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], kTileBytes + weight_tile_tx<KIND>());
-          tma_load_2d(sa, &tm_a, ks * 128, b * kBM, &full[slot]);
-          tma_load_3d(sb, &tm_b, ks * 128, nt * kBN, e, &full[slot]);
+          // row scales: stored in tcgen05.cp chunks per 128-row tile already
+          for (int c = 0; c < nchunk; ++c)
+            bulk_g2s(smem + TcLayout::sfa + slot * 1024 + 512 * c,
+                     p.as + ((size_t)b * (nblk_k / 4) + (ks * KD::kBlocks) / 4 + c) * 512, 512u, &full[slot]);
         }
       }
-    }
-    if (STAGE == 1 && pending >= 0) {
-      cp_async_wait0();
-      fence_proxy_async();
-      mbar_arrive(&full[pending]);
     }
   } else if (warp == 1) {
-    // ------------------------------ scale copies ------------------------------
+    // ---------------- weight scales: staging (row-major) -> tcgen05.cp chunks ----------------
+    const int sb_row = kdim / 32;
     uint32_t stage = 0;
-    int pending = -1;  // slot whose copies are issued but not yet signalled
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int b = tile / ntn, nt = tile % ntn;
-      const int e = p.block_expert[b];
-      const uint8_t* arow[4];
-      const uint8_t* brow[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int m = 4 * lane + i;
-        if (STAGE == 1) {
-          const int pid = p.sorted_ids[b * kBM + m];
-          arow[i] = p.as + (size_t)(pid < TK ? pid / K : 0) * p.xs_stride;
-          const int wr = m < 64 ? nt * 64 + m : I + nt * 64 + (m - 64);
-          brow[i] = p.wscale + ((size_t)e * 2 * I + wr) * (H / 32);
-        } else {
-          arow[i] = nullptr;
-          brow[i] = p.wscale + ((size_t)e * H + (size_t)nt * kBN + m) * (I / 32);
-        }
-      }
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      const int tp = lt & 1;
+      if (!mbar_wait_or_abort(&wsfull[tp], (lt >> 1) & 1, p.err, &abort_flag)) break;
+      const uint8_t* wst = smem + TcLayout::ws + tp * TcLayout::ws_bytes;
       for (int ks = 0; ks < ktiles; ++ks, ++stage) {
         const int slot = stage % kNS;
         if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
@@ -238,39 +209,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         for (int c = 0; c < KD::kChunks; ++c) {
           const int kb0 = ks * KD::kBlocks + 4 * c;  // first 32-block of this chunk
           const bool in = kb0 < nblk_k;              // kdim % 128 == 0: a chunk is all in or all out
-          if (STAGE == 1) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int m = 4 * lane + i;
-              if (in) cp_async4(dA + 512 * c + sf_off(m), arow[i] + kb0);
-              else *reinterpret_cast<uint32_t*>(dA + 512 * c + sf_off(m)) = 0x7F7F7F7Fu;
-            }
-          } else {
-            // intermediate scales are stored by stage 1 already in chunk layout
-            const uint8_t* src = p.as + ((size_t)b * (nblk_k / 4) + (kb0 / 4)) * 512 + 16 * lane;
-            if (in) cp_async16(dA + 512 * c + 16 * lane, src);
-            else *reinterpret_cast<uint4*>(dA + 512 * c + 16 * lane) = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          }
+          if (!in)  // past the end of K: neutral scales (the operands there are zero)
+            *reinterpret_cast<uint4*>(dA + 512 * c + 16 * lane) =
+                make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int m = 4 * lane + i;
-            if (in) cp_async4(dB + 512 * c + sf_off(m), brow[i] + kb0);
-            else *reinterpret_cast<uint32_t*>(dB + 512 * c + sf_off(m)) = 0x7F7F7F7Fu;
+            *reinterpret_cast<uint32_t*>(dB + 512 * c + sf_off(m)) =
+                in ? *reinterpret_cast<const uint32_t*>(wst + m * sb_row + kb0) : 0x7F7F7F7Fu;
           }
         }
-        cp_async_commit();
-        if (pending >= 0) {
-          cp_async_wait1();     // everything but the group just committed has landed
-          fence_proxy_async();  // generic-proxy writes -> visible to tcgen05.cp
-          mbar_arrive(&full[pending]);
-        }
-        pending = slot;
+        fence_proxy_async();  // generic smem writes -> visible to tcgen05.cp
+        mbar_arrive(&full[slot]);
       }
-    }
-    if (pending >= 0) {
-      cp_async_wait0();
-      fence_proxy_async();
-      mbar_arrive(&full[pending]);
+      __syncwarp();
+      mbar_arrive(&wsempty[tp]);
     }
   } else if (warp == 2) {
     // ------------------------------ MMA issuer ------------------------------

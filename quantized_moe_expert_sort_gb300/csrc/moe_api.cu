@@ -69,6 +69,8 @@ struct moe_ctx {
   int hist_chunks;
   int32_t *sorted_ids, *block_expert, *expert_count, *expert_offset, *active_experts, *meta, *hist;
   uint8_t *xq, *xs, *inter_q, *inter_s;
+  uint8_t *xq_sorted, *xs_sorted;  // tensor-core path: activations in sorted order + chunked scales
+  int32_t* pair_row;
   float* acc32;
   int* err;
   void* st_x;
@@ -103,6 +105,7 @@ static void prof_mark(moe_ctx* c, cudaStream_t st, const char* name) {
 static void free_ctx(moe_ctx* c) {
   void* ptrs[] = {c->sorted_ids, c->block_expert, c->expert_count, c->expert_offset, c->active_experts,
                   c->meta, c->hist, c->xq, c->xs, c->inter_q, c->inter_s, c->acc32, c->err,
+                  c->xq_sorted, c->xs_sorted, c->pair_row,
                   c->st_x, c->st_ids, c->st_w, c->st_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -279,6 +282,9 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->inter_q, (size_t)c->cap_rows * I * 2},
       {(void**)&c->inter_s, (size_t)c->cap_rows * scale_row_stride(I)},
       {(void**)&c->acc32, sizeof(float) * (size_t)max_tokens * H},
+      {(void**)&c->xq_sorted, (size_t)c->cap_rows * H},
+      {(void**)&c->xs_sorted, (size_t)c->cap_rows * H / 32},
+      {(void**)&c->pair_row, sizeof(int32_t) * pairs},
       {(void**)&c->err, sizeof(int) * 4},
       {(void**)&c->st_x, (size_t)max_tokens * H * 2},
       {(void**)&c->st_ids, sizeof(int32_t) * pairs},
@@ -373,10 +379,11 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   // number of routed rows per active expert reaches tc_min_rows; the decode
   // kernels (8-row groups, register-dequantised weights) below that and for
   // bf16 activations.
-  const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active;
+  const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active &&
+                      c->H <= TC_MAX_K && c->I <= TC_MAX_K;
   const int tile_m = use_tc ? TC_TILE_M : kDecodeTile;
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
-  CUtensorMap tm_inter;
+  CUtensorMap tm_inter, tm_xs;
   moe_status ms;
   if (use_tc) {
     ms = make_w13tc_map(c, w13, kind);
@@ -388,6 +395,10 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     cuuint32_t ibox[2] = {128, 128};
     ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate");
     if (ms != MOE_OK) return ms;
+    const cuuint64_t xrow = adt == MOE_A_FP8 ? (cuuint64_t)c->H : (cuuint64_t)c->H / 2;
+    cuuint64_t xdims[2] = {xrow, (cuuint64_t)c->cap_rows}, xstr[1] = {xrow};
+    ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activations");
+    if (ms != MOE_OK) return ms;
   } else {
     ms = make_w13_map(c, w13);
     if (ms != MOE_OK) return ms;
@@ -397,12 +408,17 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
 
   c->ev_n = 0;
   prof_mark(c, st, "sort");
-  cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, sort_out(c), c->hist, c->hist_chunks, c->err, st);
+  SortOut so = sort_out(c);
+  if (use_tc) so.pair_row = c->pair_row;
+  cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
   if (e != cudaSuccess) return cuda_fail(e, "sort launch");
   c->last_tile_m = tile_m;
   c->last_inter_layout = use_tc ? 1 : 0;
   prof_mark(c, st, "act_quant");
-  e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
+  if (use_tc)
+    e = launch_act_quant_sorted(x, T, c->H, c->K, fmt, c->pair_row, c->xq_sorted, c->xs_sorted, c->acc32, c->num_sms, st);
+  else
+    e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
 
   StageParams p{};
@@ -430,7 +446,10 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   if (use_tc) {
     long t1 = max_blocks * (c->I / 64), t2 = max_blocks * (c->H / 128);
     prof_mark(c, st, "stage1");
-    e = launch_tc_stage(kind, 1, p1, tm_inter /* unused by stage 1 */, c->tm_w13tc, (int)(t1 < c->num_sms ? t1 : c->num_sms), st);
+    StageParams q1 = p1;
+    q1.aq = c->xq_sorted;
+    q1.as = c->xs_sorted;
+    e = launch_tc_stage(kind, 1, q1, tm_xs, c->tm_w13tc, (int)(t1 < c->num_sms ? t1 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     prof_mark(c, st, "stage2");
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
