@@ -101,10 +101,13 @@ typedef struct {
 } moe_sort_view;
 
 /* Workspace view for inspection (tests, debugging): device pointers owned by ctx.
- * inter_codes rows follow the sorted order of the last moe_forward (tile_m 8 on
- * the decode path, 128 on the tensor-core path); the element format is that of
- * its a_dtype: bf16 -> f16 codes (2 bytes, block-scaled re-encoding of the bf16
- * intermediate), fp8 -> e4m3 bytes, fp4 -> e2m1 pairs. */
+ * inter_codes rows follow the sorted order of the last moe_forward (sort.tile_m
+ * gives its padding: 1 on the few-rows tensor-core path, 128 on the many-rows
+ * one); the element format follows its a_dtype: fp8 -> e4m3 bytes, fp4 -> e2m1
+ * pairs, bf16 -> layout 2 below (a pair of e4m3 codes whose sum is the bf16
+ * intermediate). act_codes / act_scales hold per-token codes only after
+ * moe_quantize_activations-style use; the forward writes activations straight
+ * into sorted order. */
 typedef struct {
   moe_sort_view sort;
   uint8_t* act_codes;      /* [max_tokens, H * bytes/elt] */
@@ -113,11 +116,14 @@ typedef struct {
   uint8_t* inter_scales;   /* [max_rows, inter_scale_stride] (first I/32 bytes of a row used) */
   float* acc32;            /* [max_tokens, H] fp32 combine buffer */
   int32_t act_scale_stride;   /* H/32 rounded up to 16 */
-  int32_t inter_scale_stride; /* I/32 rounded up to 16 */
+  int32_t inter_scale_stride; /* bytes per scale row: I/32 (2I/32 for layout 2) rounded up to 16 */
   int32_t inter_scale_layout; /* 0: row-major [rows, inter_scale_stride];
                                  1: per 128-row tile b and 4-block chunk c, 512 bytes at
                                     (b * I/128 + c) * 512, byte 16*(m%32) + 4*(m/32) + kb%4
-                                    for tile row m and 32-block kb (tensor-core path) */
+                                    for tile row m and 32-block kb (many-rows path);
+                                 2: hi / lo e4m3 pairs: codes [rows, 2I] (hi in bytes [0, I),
+                                    lo in [I, 2I)), scales row-major [rows, inter_scale_stride]
+                                    (hi in [0, I/32), lo in [I/32, 2I/32)); value = hi + lo */
 } moe_workspace_view;
 
 /* Create a context on `device` for fixed (hidden, inter, num_experts, topk) and

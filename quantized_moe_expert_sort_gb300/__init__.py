@@ -201,9 +201,19 @@ class MoE:
         return self._sort_dict(self.workspace().sort)
 
     def intermediate(self, rows, a_dtype):
-        """Copies of the stage-1 output rows [rows, I] codes and [rows, I/32] scales."""
+        """Copies of the stage-1 output rows of the last forward: (codes, scales, fmt).
+
+        fmt 'f16' / 'e4m3' / 'e2m1': codes [rows, I * bytes per element], scales [rows, I/32].
+        fmt 'e4m3_hilo' (bf16 activations on the tensor-core path): codes [rows, 2I] and
+        scales [rows, 2I/32], hi in the first half of each, lo in the second; value = hi + lo.
+        """
         v = self.workspace()
+        if v.inter_scale_layout == 2:
+            codes = _view(v.inter_codes, (rows, 2 * self.I), torch.uint8).clone()
+            scales = _view(v.inter_scales, (rows, v.inter_scale_stride), torch.uint8)[:, :2 * self.I // 32].clone()
+            return codes, scales, "e4m3_hilo"
         bpe = {"bf16": 2, "fp8": 1, "fp4": 0.5}[a_dtype]
+        fmt = {"bf16": "f16", "fp8": "e4m3", "fp4": "e2m1"}[a_dtype]
         codes = _view(v.inter_codes, (rows, int(self.I * bpe)), torch.uint8).clone()
         if v.inter_scale_layout == 0:
             scales = _view(v.inter_scales, (rows, v.inter_scale_stride), torch.uint8)[:, :self.I // 32].clone()
@@ -211,7 +221,7 @@ class MoE:
             nb, nc = rows // 128, self.I // 128
             raw = _view(v.inter_scales, (nb, nc, 32, 4, 4), torch.uint8)  # [tile, chunk, m%32, m/32, kb%4]
             scales = raw.permute(0, 3, 2, 1, 4).reshape(rows, self.I // 32).clone()
-        return codes, scales
+        return codes, scales, fmt
 
     def set_profiling(self, enable=True):
         _check(lib().moe_set_profiling(self._h, 1 if enable else 0))

@@ -76,6 +76,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return (uint32_t)out;
 }
 
+// One e4m3 code (low byte) -> its value as fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(h) : "r"(code & 0xFFu));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
 // Eight e2m1 codes (nibble i = element i) -> four f16x2 words; word j holds
 // elements 2j (low half) and 2j+1 (high half).
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
@@ -97,12 +104,24 @@ __device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t w, uint32_t& even, uint3
 
 // ---------------------------------------------------------------------------
 // Activation functions (aiter PR 6259 Motivation, PR 4471 Motivation)
+// sigmoid(z) = 1 / (1 + 2^(-z * log2 e)) with the hardware exp2 and reciprocal;
+// tanh(z) = 2 * sigmoid(2z) - 1, the identity the int4 SiTUv2 page builds tanh
+// from: it saturates to +-1 at both ends without clamping.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_sigmoid(float z) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * z));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+
+__device__ __forceinline__ float fast_tanh(float z) { return 2.0f * fast_sigmoid(2.0f * z) - 1.0f; }
+
 __device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta) {
-  float sig = 1.0f / (1.0f + __expf(-g));
+  const float sig = fast_sigmoid(g);
   if (act == ACT_SILU) return g * sig * u;
-  float situ = beta * tanhf(g / beta) * sig;
-  float up = lbeta * tanhf(u / lbeta);
+  const float situ = beta * fast_tanh(g / beta) * sig;
+  const float up = lbeta * fast_tanh(u / lbeta);
   return situ * up;
 }
 
@@ -148,7 +167,7 @@ __device__ __forceinline__ void block_store_lane(uint8_t* dst, uint32_t code, in
   }
 }
 
-__device__ __forceinline__ int fmt_bytes_per_32(int fmt) { return fmt == FMT_F16 ? 64 : (fmt == FMT_E4M3 ? 32 : 16); }
+__host__ __device__ __forceinline__ int fmt_bytes_per_32(int fmt) { return fmt == FMT_F16 ? 64 : (fmt == FMT_E4M3 ? 32 : 16); }
 
 // ---------------------------------------------------------------------------
 // mbarrier / TMA (inline PTX). Every wait is bounded: on timeout it records

@@ -35,12 +35,22 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
 cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t st);
 cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
-// Activation quantisation written straight into sorted order (tensor-core path):
-// codes of pair p's row go to row pair_row[p] of xq_sorted (row_bytes apart),
-// its e8m0 scales into 512-byte tcgen05.cp chunks per 128-row tile.
+// Activation quantisation for the tensor-core path: quantise each token once
+// (xq / xs, row-major), then copy each routed pair's row to its sorted row
+// pair_row[p] of xq_sorted and its e8m0 scales into 512-byte tcgen05.cp chunks
+// per 128-row tile.
 cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
-                                    uint8_t* xq_sorted, uint8_t* xs_chunks, float* acc32, int num_sms,
-                                    cudaStream_t st);
+                                    uint8_t* xq, uint8_t* xs, int xs_stride, uint8_t* xq_sorted, uint8_t* xs_chunks,
+                                    float* acc32, int num_sms, cudaStream_t st);
+
+// Activation quantisation for the few-rows-per-expert tensor-core path: each
+// token's row is quantised once (one thread per 32-block) and written straight
+// to the sorted rows of its routed pairs, codes [rows, row_bytes] and e8m0
+// scales [rows, scale_stride], both row-major. mode SW_A8: e4m3; SW_A4: e2m1;
+// SW_A16: the pair (hi, lo) of e4m3 codes whose sum carries the bf16 value
+// (hi in bytes [0, H) of a row, lo in [H, 2H); scales hi in [0, H/32), lo after).
+cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
+                               uint8_t* scales, int scale_stride, float* acc32, int num_sms, cudaStream_t st);
 
 // Parameters of the grouped stage kernels (decode family).
 struct StageParams {
@@ -62,6 +72,7 @@ struct StageParams {
   float* acc32;       // stage 2: [T, H]
   const float* topk_w;  // stage 2: [T*K]
   int xs_stride;       // bytes per row of the activation-scale array (as)
+  int aq_stride;       // bytes per row of the activation-code array (few-rows tensor-core path)
   int os_stride;       // stage 1: bytes per row of the output-scale array (os)
   int T, H, I, E, K;
   int act;
@@ -83,6 +94,13 @@ using TcParams = StageParams;
 cudaError_t tc_set_smem_limits();
 cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                             int grid, cudaStream_t st);
+
+// tcgen05 family for few routed rows per expert (decode): the weight tile is
+// the M = 128 operand and the expert's routed rows the N <= 64 operand.
+enum { SW_A16 = 0, SW_A8 = 1, SW_A4 = 2 };
+cudaError_t swap_set_smem_limits();
+cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                              int grid, cudaStream_t st);
 
 cudaError_t decode_set_smem_limits();
 int decode_s1_blocks_per_sm(int fmt, int H);

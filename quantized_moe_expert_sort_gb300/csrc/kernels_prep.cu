@@ -314,40 +314,151 @@ __global__ void __launch_bounds__(256) act_encode_f16_kernel(const __nv_bfloat16
   }
 }
 
-// Activation quantisation into sorted order for the tensor-core path: one warp
-// per (token, 32-block); the block's codes are written to the sorted row of
-// every routed pair of the token, its scale byte into the tile's 512-byte
-// chunk (byte 16*(m%32) + 4*(m/32) + b%4 of chunk b/4, m = row % 128).
-__global__ void __launch_bounds__(256) act_quant_sorted_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
-                                                               int fmt, const int32_t* __restrict__ pair_row,
-                                                               uint8_t* __restrict__ xq_sorted,
-                                                               uint8_t* __restrict__ xs_chunks,
-                                                               float* __restrict__ acc32) {
+// Copy of the quantised activation rows into sorted order for the tensor-core
+// path: one warp per routed pair p, whose token's row (quantised once per token
+// by act_quant_kernel) goes to sorted row r = pair_row[p] with 16-byte stores;
+// its e8m0 scales go into the tile's 512-byte tcgen05.cp chunks (byte
+// 16*(m%32) + 4*(m/32) + b%4 of chunk b/4, m = r % 128).
+__global__ void __launch_bounds__(256) act_gather_sorted_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs,
+                                                                int xs_stride, long pairs, int K, int nb, int row_bytes,
+                                                                const int32_t* __restrict__ pair_row,
+                                                                uint8_t* __restrict__ xq_sorted,
+                                                                uint8_t* __restrict__ xs_chunks) {
   const int lane = threadIdx.x & 31;
   const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
-  const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nv = row_bytes / 16;  // 16-byte pieces per row (<= 256 for H <= 4096)
+  for (long pr = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < pairs; pr += nwarps) {
+    const int r = pair_row[pr];
+    if (r < 0) continue;  // dropped pair (warp-uniform)
+    const long t = pr / K;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + t * (long)row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(xq_sorted + (size_t)r * row_bytes);
+    // all loads first (independent, in flight together), then the stores
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < nv) v[i] = __ldg(src + lane + 32 * i);
+    // scales: one 32-bit word = 4 consecutive 32-blocks = one chunk's bytes for this row
+    const int nw = nb / 4;
+    uint32_t sw[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (lane + 32 * i < nw) sw[i] = __ldg(reinterpret_cast<const uint32_t*>(xs + t * xs_stride) + lane + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < nv) dst[lane + 32 * i] = v[i];
+    const int m = r & 127;
+    uint8_t* ch = xs_chunks + (size_t)(r >> 7) * nw * 512 + 16 * (m & 31) + 4 * (m >> 5);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (lane + 32 * i < nw) *reinterpret_cast<uint32_t*>(ch + (size_t)(lane + 32 * i) * 512) = sw[i];
+  }
+}
+
+// Thread-local 1x32 scale: amax -> (e8m0 byte, multiplier 2^-E) with
+// E = floor(log2 amax) - emax clamped to [-127, 127]; amax == 0 -> byte 127, 0.
+__device__ __forceinline__ uint32_t block_scale_of(float amax, int emax, float* mul) {
+  if (!(amax > 0.0f)) {
+    *mul = 0.0f;
+    return 127u;
+  }
+  int E = floor_log2_f32(amax) - emax;
+  E = E < -127 ? -127 : (E > 127 ? 127 : E);
+  *mul = exp2_neg(E);
+  return (uint32_t)(E + 127);
+}
+
+// Quantise one token's 32-block per thread and write it to the sorted rows of
+// the token's K routed pairs (see launch_act_scatter).
+template <int MODE>
+__global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+                                                          const int32_t* __restrict__ pair_row,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                          int sstride, float* __restrict__ acc32) {
   const int nb = H / 32;
-  const int bpb = fmt_bytes_per_32(fmt);
-  const size_t row_bytes = (size_t)nb * bpb;
-  for (long blk = gw; blk < (long)T * nb; blk += nwarps) {
-    const long t = blk / nb;
-    const int b = (int)(blk % nb);
-    const float v = __bfloat162float(x[t * H + b * 32 + lane]);
-    uint32_t s;
-    const uint32_t code = block_quant_lane(v, fmt, &s);
+  const long total = (long)T * nb;
+  const long row_bytes = MODE == SW_A4 ? H / 2 : (MODE == SW_A16 ? 2L * H : (long)H);
+  const long nthreads = (long)gridDim.x * blockDim.x;
+  for (long w = (long)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += nthreads) {
+    const long t = w / nb;
+    const int b = (int)(w % nb);
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + 32 * b);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = __ldg(src + i);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * i + 2 * j] = __uint_as_float(wd[j] << 16);
+        v[8 * i + 2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    uint32_t c0[8], c1[8];  // codes: MODE A8 / A16-hi in c0, A16-lo in c1, A4 in c0[0..3]
+    uint32_t s0, s1 = 127u;
+    float mul;
+    if (MODE == SW_A4) {
+      s0 = block_scale_of(amax, 2, &mul);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          acc |= cvt_e2m1x2(__fmul_rn(v[8 * i + 2 * k], mul), __fmul_rn(v[8 * i + 2 * k + 1], mul)) << (8 * k);
+        c0[i] = acc;
+      }
+    } else {
+      // A8: the MX rule (emax 8, saturating). A16 hi: emax 7, so that no code saturates.
+      s0 = block_scale_of(amax, MODE == SW_A16 ? 7 : 8, &mul);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        c0[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul), __fmul_rn(v[4 * i + 1], mul)) |
+                (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul), __fmul_rn(v[4 * i + 3], mul)) << 16);
+      if (MODE == SW_A16) {
+        // lo: the exact residual v - hi * 2^E, quantised the same way
+        const float inv = e8m0_to_f32(s0);  // 2^E (codes are 0 for an all-zero block)
+        float rmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float hv = e4m3_to_f32((c0[i >> 2] >> (8 * (i & 3))) & 0xFFu) * inv;
+          v[i] = v[i] - hv;
+          rmax = fmaxf(rmax, fabsf(v[i]));
+        }
+        float mul1;
+        s1 = block_scale_of(rmax, 7, &mul1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          c1[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul1), __fmul_rn(v[4 * i + 1], mul1)) |
+                  (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul1), __fmul_rn(v[4 * i + 3], mul1)) << 16);
+      }
+    }
     for (int k = 0; k < K; ++k) {
-      const int r = pair_row[t * K + k];
-      if (r < 0) continue;  // dropped pair (warp-uniform)
-      block_store_lane(xq_sorted + (size_t)r * row_bytes + (size_t)b * bpb, code, fmt, lane);
-      if (lane == 0)
-        xs_chunks[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (b & 3)] =
-            (uint8_t)s;
+      const int r = __ldg(pair_row + t * K + k);
+      if (r < 0) continue;
+      uint8_t* dst = codes + (size_t)r * row_bytes;
+      if (MODE == SW_A4) {
+        *reinterpret_cast<uint4*>(dst + 16 * b) = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+      } else {
+        uint4* d0 = reinterpret_cast<uint4*>(dst + 32 * b);
+        d0[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+        d0[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
+        if (MODE == SW_A16) {
+          uint4* d1 = reinterpret_cast<uint4*>(dst + H + 32 * b);
+          d1[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+          d1[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+        }
+      }
+      scales[(size_t)r * sstride + b] = (uint8_t)s0;
+      if (MODE == SW_A16) scales[(size_t)r * sstride + nb + b] = (uint8_t)s1;
     }
   }
   if (acc32) {
-    long n4 = (long)T * H / 4;
-    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
+    const long n4 = (long)T * H / 4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += nthreads)
       reinterpret_cast<float4*>(acc32)[i] = z;
   }
 }
@@ -432,15 +543,37 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
 }
 
 cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
-                                    uint8_t* xq_sorted, uint8_t* xs_chunks, float* acc32, int num_sms,
-                                    cudaStream_t st) {
-  long work = (long)T * (H / 32);
-  long blocks = (work + 7) / 8;
+                                    uint8_t* xq, uint8_t* xs, int xs_stride, uint8_t* xq_sorted, uint8_t* xs_chunks,
+                                    float* acc32, int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_act_quant(x, T, H, fmt, xq, xs, xs_stride, acc32, num_sms, st);
+  if (e != cudaSuccess) return e;
+  const long pairs = (long)T * K;
+  long blocks = (pairs + 7) / 8;
   long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  act_quant_sorted_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), T, H, K, fmt,
-                                                       pair_row, xq_sorted, xs_chunks, acc32);
+  const int row_bytes = H / 32 * fmt_bytes_per_32(fmt);
+  act_gather_sorted_kernel<<<(int)blocks, 256, 0, st>>>(xq, xs, xs_stride, pairs, K, H / 32, row_bytes, pair_row,
+                                                        xq_sorted, xs_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
+                               uint8_t* scales, int scale_stride, float* acc32, int num_sms, cudaStream_t st) {
+  const long work = (long)T * (H / 32);
+  long blocks = (work + 127) / 128;
+  const long floor_blocks = ((long)T * H / 4 + 127) / 128;  // enough threads to zero acc32 quickly
+  if (blocks < floor_blocks / 4) blocks = floor_blocks / 4;
+  const long cap = (long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (mode == SW_A16)
+    act_scatter_kernel<SW_A16><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
+  else if (mode == SW_A8)
+    act_scatter_kernel<SW_A8><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
+  else
+    act_scatter_kernel<SW_A4><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,8 @@
 namespace moe {
 namespace {
 
-constexpr int kThreadsTc = 256;
+constexpr int kThreadsTc = 384;        // warps 0-3 producer / scales / MMA / idle, 4-11 epilogue
+constexpr int kEpiWarps = 8;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
 constexpr int kNS = 4;          // pipeline stages
@@ -66,7 +67,9 @@ struct TcLayout {
   static constexpr uint32_t sfb = sfa + kNS * 1024;
   static constexpr uint32_t ws = sfb + kNS * 1024;                 // 2 x weight-scale staging
   static constexpr uint32_t ws_bytes = 128 * 128;                  // 128 rows x up to 128 scale bytes (K <= 4096)
-  static constexpr uint32_t bars = ws + 2 * ws_bytes;
+  static constexpr uint32_t epi = ws + 2 * ws_bytes;               // stage-2 transpose: per epilogue warp 32 x 36 fp32
+  static constexpr uint32_t epi_bytes = 32 * 36 * 4;
+  static constexpr uint32_t bars = epi + kEpiWarps * epi_bytes;
   static constexpr uint32_t tmem_slot = bars + (2 * kNS + 8) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;        // + alignment slack
 };
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
     for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 4);
+      mbar_init(&tempty[s], kEpiWarps);
       mbar_init(&wsfull[s], 1);
       mbar_init(&wsempty[s], 32);
     }
@@ -269,7 +272,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
     }
   } else if (warp >= 4) {
     // ------------------------------ epilogue ------------------------------
-    const int q = warp & 3;
+    const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    const int grp = (warp - 4) >> 2;       // column group: 0 -> warps 4-7, 1 -> warps 8-11
     const int m = 32 * q + lane;           // tile row of this thread (= TMEM lane)
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     int lt = 0;
@@ -284,8 +288,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
       tc::fence_after();
       const uint32_t d = tbase + lane_off + buf * kBN;
       if (STAGE == 1) {
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        {
+          const int h = grp;  // the group's 32 intermediate columns
           uint32_t gr[32], ur[32];
           tc::ld_32x32b_x16(d + 32 * h, gr);
           tc::ld_32x32b_x16(d + 32 * h + 16, gr + 16);
@@ -343,21 +347,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           }
         }
       } else {
+        // Each thread holds row m (one routed pair) x 32 columns of H. The warp
+        // transposes them through shared memory so that one vector red covers
+        // 4 rows x 128 contiguous bytes instead of 32 rows x 16 bytes.
         const int t = valid ? pid / K : 0;
         const float wt = valid ? p.topk_w[pid] : 0.0f;
-        float* dst = p.acc32 + (size_t)t * H + (size_t)nt * kBN;
+        float* tb = reinterpret_cast<float*>(smem + TcLayout::epi + (warp - 4) * TcLayout::epi_bytes);
+        const unsigned vmask = __ballot_sync(0xFFFFFFFFu, valid);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
           uint32_t r[32];
           tc::ld_32x32b_x16(d + 32 * c, r);
           tc::ld_32x32b_x16(d + 32 * c + 16, r + 16);
           tc::ld_wait();
-          if (valid) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              red_add_v4(dst + 32 * c + 4 * i, wt * __uint_as_float(r[4 * i]), wt * __uint_as_float(r[4 * i + 1]),
-                         wt * __uint_as_float(r[4 * i + 2]), wt * __uint_as_float(r[4 * i + 3]));
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(tb + lane * 36 + 4 * i) =
+                make_float4(wt * __uint_as_float(r[4 * i]), wt * __uint_as_float(r[4 * i + 1]),
+                            wt * __uint_as_float(r[4 * i + 2]), wt * __uint_as_float(r[4 * i + 3]));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);  // row of the warp this lane adds for
+            const int tr = __shfl_sync(0xFFFFFFFFu, t, rr);
+            if ((vmask >> rr) & 1u) {
+              const float4 v = *reinterpret_cast<const float4*>(tb + rr * 36 + 4 * (lane & 7));
+              red_add_v4(p.acc32 + (size_t)tr * H + (size_t)nt * kBN + 32 * c + 4 * (lane & 7), v.x, v.y, v.z, v.w);
+            }
           }
+          __syncwarp();
         }
       }
       tc::fence_before();

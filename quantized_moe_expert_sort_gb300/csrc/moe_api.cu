@@ -85,6 +85,9 @@ struct moe_ctx {
   // tcgen05 family maps (keyed by pointer and kind)
   const void* tm_w13tc_key; int tm_w13tc_kind; CUtensorMap tm_w13tc;
   const void* tm_w2tc_key; int tm_w2tc_kind; CUtensorMap tm_w2tc;
+  const void* tm_w13sw_key; int tm_w13sw_kind; CUtensorMap tm_w13sw;  // 128-row gate / up tiles
+  int legacy_decode;  // MOE_DECODE_LEGACY=1: register-dequantising decode kernels for few rows per expert
+  int last_inter_stride;
   int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
   int last_inter_layout;
   int last_tile_m;
@@ -199,6 +202,26 @@ static moe_status make_w2tc_map(moe_ctx* c, const uint8_t* w2, int kind) {
   return MOE_OK;
 }
 
+// Stage-1 weights of the few-rows tensor-core path: 128 gate (or up) rows per box.
+static moe_status make_w13sw_map(moe_ctx* c, const uint8_t* w13, int kind) {
+  if (c->tm_w13sw_key == w13 && c->tm_w13sw_kind == kind) return MOE_OK;
+  const cuuint64_t H = c->H, I = c->I, E = c->E;
+  cuuint64_t strides[3] = {H / 2, I * H / 2, 2 * I * H / 2};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  moe_status s;
+  if (kind == TC_A8W4) {
+    cuuint64_t dims[4] = {H, I, 2, E};
+    s = encode(&c->tm_w13sw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, w13, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w13 fp4 unpacked, 128 rows");
+  } else {
+    cuuint64_t dims[4] = {H / 2, I, 2, E};
+    s = encode(&c->tm_w13sw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, w13, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "w13 fp4 packed, 128 rows");
+  }
+  if (s != MOE_OK) return s;
+  c->tm_w13sw_key = w13;
+  c->tm_w13sw_kind = kind;
+  return MOE_OK;
+}
+
 static SortOut sort_out(moe_ctx* c) {
   SortOut so;
   so.sorted_ids = c->sorted_ids;
@@ -280,10 +303,10 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->xq, (size_t)max_tokens * H * 2},
       {(void**)&c->xs, (size_t)max_tokens * scale_row_stride(H)},
       {(void**)&c->inter_q, (size_t)c->cap_rows * I * 2},
-      {(void**)&c->inter_s, (size_t)c->cap_rows * scale_row_stride(I)},
+      {(void**)&c->inter_s, (size_t)c->cap_rows * scale_row_stride(2 * I)},
       {(void**)&c->acc32, sizeof(float) * (size_t)max_tokens * H},
-      {(void**)&c->xq_sorted, (size_t)c->cap_rows * H},
-      {(void**)&c->xs_sorted, (size_t)c->cap_rows * H / 32},
+      {(void**)&c->xq_sorted, (size_t)c->cap_rows * H * 2},
+      {(void**)&c->xs_sorted, (size_t)c->cap_rows * scale_row_stride(2 * H)},
       {(void**)&c->pair_row, sizeof(int32_t) * pairs},
       {(void**)&c->err, sizeof(int) * 4},
       {(void**)&c->st_x, (size_t)max_tokens * H * 2},
@@ -304,12 +327,15 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   if (e == cudaSuccess) e = prep_set_smem_limits();
   if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e == cudaSuccess) e = tc_set_smem_limits();
+  if (e == cudaSuccess) e = swap_set_smem_limits();
   if (e != cudaSuccess) {
     free_ctx(c);
     return cuda_fail(e, "context setup");
   }
   c->tc_min_rows = 32;
   if (const char* v = getenv("MOE_TC_MIN_ROWS")) c->tc_min_rows = atoi(v);
+  if (const char* v = getenv("MOE_DECODE_LEGACY")) c->legacy_decode = atoi(v);
+  c->last_inter_stride = scale_row_stride(I);
   for (int f = 0; f < 3; ++f) {
     c->s1_bps[f] = decode_s1_blocks_per_sm(f, H);
     c->s2_bps[f] = decode_s2_blocks_per_sm(f, I);
@@ -335,7 +361,7 @@ moe_status moe_get_workspace(moe_ctx* c, moe_workspace_view* v) {
   v->inter_scales = c->inter_s;
   v->acc32 = c->acc32;
   v->act_scale_stride = scale_row_stride(c->H);
-  v->inter_scale_stride = scale_row_stride(c->I);
+  v->inter_scale_stride = c->last_inter_stride;
   v->inter_scale_layout = c->last_inter_layout;
   return MOE_OK;
 }
@@ -375,14 +401,23 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   const int fmt = fmt_of_adtype(adt);
   const long pairs = (long)T * c->K;
   const long max_active = pairs < c->E ? pairs : c->E;
-  // Path: the tcgen05 kernels (128-row tiles of one expert) once the mean
-  // number of routed rows per active expert reaches tc_min_rows; the decode
-  // kernels (8-row groups, register-dequantised weights) below that and for
-  // bf16 activations.
+  // Path: the many-rows tcgen05 kernels (128 routed rows x 128 weight rows per
+  // tile) once the mean number of routed rows per active expert reaches
+  // tc_min_rows (fp8 / fp4 activations); below that the few-rows tcgen05
+  // kernels (128 weight rows x up to 64 routed rows per MMA).
   const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active &&
                       c->H <= TC_MAX_K && c->I <= TC_MAX_K;
-  const int tile_m = use_tc ? TC_TILE_M : kDecodeTile;
+  const bool use_legacy = !use_tc && c->legacy_decode;
+  const bool use_sw = !use_tc && !use_legacy;
+  const int tile_m = use_tc ? TC_TILE_M : (use_sw ? 1 : kDecodeTile);
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
+  const int swkind = adt == MOE_A_BF16 ? SW_A16 : (adt == MOE_A_FP8 ? SW_A8 : SW_A4);
+  const int wkind = adt == MOE_A_FP4 ? TC_A4W4 : TC_A8W4;  // weight map type: packed for mxf4, unpacked otherwise
+  // few-rows path: row bytes of the sorted activations / intermediate and their scale strides
+  const int x_row = adt == MOE_A_BF16 ? 2 * c->H : (adt == MOE_A_FP8 ? c->H : c->H / 2);
+  const int i_row = adt == MOE_A_BF16 ? 2 * c->I : (adt == MOE_A_FP8 ? c->I : c->I / 2);
+  const int xs_sw = scale_row_stride(adt == MOE_A_BF16 ? 2 * c->H : c->H);
+  const int is_sw = scale_row_stride(adt == MOE_A_BF16 ? 2 * c->I : c->I);
   CUtensorMap tm_inter, tm_xs;
   moe_status ms;
   if (use_tc) {
@@ -399,6 +434,18 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     cuuint64_t xdims[2] = {xrow, (cuuint64_t)c->cap_rows}, xstr[1] = {xrow};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activations");
     if (ms != MOE_OK) return ms;
+  } else if (use_sw) {
+    ms = make_w13sw_map(c, w13, wkind);
+    if (ms != MOE_OK) return ms;
+    ms = make_w2tc_map(c, w2, wkind);
+    if (ms != MOE_OK) return ms;
+    cuuint32_t box[2] = {128, 16};
+    cuuint64_t idims[2] = {(cuuint64_t)i_row, (cuuint64_t)c->cap_rows}, istr[1] = {(cuuint64_t)i_row};
+    ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, box, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate rows");
+    if (ms != MOE_OK) return ms;
+    cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows}, xstr[1] = {(cuuint64_t)x_row};
+    ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, box, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activation rows");
+    if (ms != MOE_OK) return ms;
   } else {
     ms = make_w13_map(c, w13);
     if (ms != MOE_OK) return ms;
@@ -409,14 +456,19 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   c->ev_n = 0;
   prof_mark(c, st, "sort");
   SortOut so = sort_out(c);
-  if (use_tc) so.pair_row = c->pair_row;
+  if (use_tc || use_sw) so.pair_row = c->pair_row;
   cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
   if (e != cudaSuccess) return cuda_fail(e, "sort launch");
   c->last_tile_m = tile_m;
-  c->last_inter_layout = use_tc ? 1 : 0;
+  c->last_inter_layout = use_tc ? 1 : (use_sw && adt == MOE_A_BF16 ? 2 : 0);
+  c->last_inter_stride = use_sw ? is_sw : scale_row_stride(c->I);
   prof_mark(c, st, "act_quant");
   if (use_tc)
-    e = launch_act_quant_sorted(x, T, c->H, c->K, fmt, c->pair_row, c->xq_sorted, c->xs_sorted, c->acc32, c->num_sms, st);
+    e = launch_act_quant_sorted(x, T, c->H, c->K, fmt, c->pair_row, c->xq, c->xs, scale_row_stride(c->H), c->xq_sorted,
+                                c->xs_sorted, c->acc32, c->num_sms, st);
+  else if (use_sw)
+    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, xs_sw, c->acc32,
+                           c->num_sms, st);
   else
     e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
@@ -453,6 +505,21 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     prof_mark(c, st, "stage2");
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
+  } else if (use_sw) {
+    const long u1 = max_active * (c->I / 128), u2 = max_active * (c->H / 128);
+    StageParams q1 = p1;
+    q1.aq = c->xq_sorted;
+    q1.as = c->xs_sorted;
+    q1.xs_stride = xs_sw;
+    q1.os_stride = is_sw;
+    prof_mark(c, st, "stage1");
+    e = launch_swap_stage(swkind, 1, q1, c->tm_w13sw, tm_xs, (int)(u1 < c->num_sms ? u1 : c->num_sms), st);
+    if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
+    StageParams q2 = p2;
+    q2.xs_stride = is_sw;
+    prof_mark(c, st, "stage2");
+    e = launch_swap_stage(swkind, 2, q2, c->tm_w2tc, tm_inter, (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   } else {
     long items1 = max_blocks * (c->I / 32);

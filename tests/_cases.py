@@ -70,6 +70,15 @@ def to_dev(case, device="cuda"):
                 w13=t(case["w13"]), w13s=t(case["w13s"]), w2=t(case["w2"]), w2s=t(case["w2s"]))
 
 
+def decode_intermediate(codes, scales, fmt):
+    """Decode the (codes, scales, fmt) triple of MoE.intermediate() to float64."""
+    if fmt == "e4m3_hilo":
+        I = codes.shape[1] // 2
+        v = decode_codes(codes, scales, "fp8")
+        return v[:, :I] + v[:, I:]
+    return decode_codes(codes, scales, {"f16": "bf16", "e4m3": "fp8", "e2m1": "fp4"}[fmt])
+
+
 def decode_codes(codes, scales, a_dtype):
     """Decode GPU activation / intermediate codes to float64 (test-side decoder)."""
     codes = np.asarray(codes)

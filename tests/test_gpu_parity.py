@@ -11,7 +11,7 @@ import torch
 import oracle
 import quantized_moe_expert_sort_gb300 as moe
 from quantized_moe_expert_sort_gb300 import inputs
-from _cases import bf16_bits, decode_codes, make_case, oracle_forward, rel_l2, to_dev, bits_to_f64
+from _cases import bf16_bits, decode_codes, decode_intermediate, make_case, oracle_forward, rel_l2, to_dev, bits_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -126,8 +126,8 @@ def test_tiny_forward(act, a_dtype):
     # stage-1 intermediate, row by row in the GPU's sorted order
     srt = ctx.last_sort()
     rows = srt["num_rows"]
-    codes, scales = ctx.intermediate(rows, a_dtype)
-    dec = decode_codes(codes.cpu().numpy(), scales.cpu().numpy(), a_dtype)
+    codes, scales, fmt = ctx.intermediate(rows, a_dtype)
+    dec = decode_intermediate(codes.cpu().numpy(), scales.cpu().numpy(), fmt)
     sid = srt["sorted_ids"].cpu().numpy()
     valid = sid < case["T"] * case["K"]
     got = dec[valid]

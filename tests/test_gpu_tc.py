@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import quantized_moe_expert_sort_gb300 as moe
-from _cases import decode_codes, make_case, oracle_forward, rel_l2, to_dev
+from _cases import decode_codes, decode_intermediate, make_case, oracle_forward, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -51,8 +51,8 @@ def test_tc_small_full_output_and_intermediate(a_dtype, act):
     st, flags = ctx.get_error()
     assert st == 0 and flags == 0
     srt = ctx.last_sort()
-    codes, scales = ctx.intermediate(srt["num_rows"], a_dtype)
-    dec = decode_codes(codes.cpu().numpy(), scales.cpu().numpy(), a_dtype)
+    codes, scales, fmt = ctx.intermediate(srt["num_rows"], a_dtype)
+    dec = decode_intermediate(codes.cpu().numpy(), scales.cpu().numpy(), fmt)
     sid = srt["sorted_ids"].cpu().numpy()
     valid = sid < case["T"] * case["K"]
     assert rel_l2(dec[valid], inter[sid[valid]]) <= TOL
