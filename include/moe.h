@@ -82,6 +82,7 @@ typedef enum { MOE_A_BF16 = 0, MOE_A_FP8 = 1, MOE_A_FP4 = 2 } moe_adtype;
 #define MOE_DEVERR_BAD_EXPERT 1
 #define MOE_DEVERR_TIMEOUT 2
 #define MOE_DEVERR_OVERFLOW 4
+#define MOE_DEVERR_LAUNCH 8  /* a kernel got less shared memory than it needs and returned without work */
 
 /* Sort output: device pointers into the context's workspace, valid until the
  * next call on the same context. Sizes are upper bounds; the real counts live
@@ -104,7 +105,7 @@ typedef struct {
  * inter_codes rows follow the sorted order of the last moe_forward (sort.tile_m
  * gives its padding: 1 on the few-rows tensor-core path, 128 on the many-rows
  * one); the element format follows its a_dtype: fp8 -> e4m3 bytes, fp4 -> e2m1
- * pairs, bf16 -> layout 2 below (a pair of e4m3 codes whose sum is the bf16
+ * pairs, bf16 -> layout 2 below (five e2m1 code terms whose sum carries the bf16
  * intermediate). act_codes / act_scales hold per-token codes only after
  * moe_quantize_activations-style use; the forward writes activations straight
  * into sorted order. */
@@ -116,14 +117,15 @@ typedef struct {
   uint8_t* inter_scales;   /* [max_rows, inter_scale_stride] (first I/32 bytes of a row used) */
   float* acc32;            /* [max_tokens, H] fp32 combine buffer */
   int32_t act_scale_stride;   /* H/32 rounded up to 16 */
-  int32_t inter_scale_stride; /* bytes per scale row: I/32 (2I/32 for layout 2) rounded up to 16 */
+  int32_t inter_scale_stride; /* bytes per scale (sub-)row: I/32 rounded up to 16 */
   int32_t inter_scale_layout; /* 0: row-major [rows, inter_scale_stride];
                                  1: per 128-row tile b and 4-block chunk c, 512 bytes at
                                     (b * I/128 + c) * 512, byte 16*(m%32) + 4*(m/32) + kb%4
                                     for tile row m and 32-block kb (many-rows path);
-                                 2: hi / lo e4m3 pairs: codes [rows, 2I] (hi in bytes [0, I),
-                                    lo in [I, 2I)), scales row-major [rows, inter_scale_stride]
-                                    (hi in [0, I/32), lo in [I/32, 2I/32)); value = hi + lo */
+                                 2: five e2m1 code terms per value, term t of row r stored as
+                                    sub-row 5r + t: codes [5 rows, I/2] (two codes per byte),
+                                    scales [5 rows, inter_scale_stride]; value = sum of the five
+                                    terms */
 } moe_workspace_view;
 
 /* Create a context on `device` for fixed (hidden, inter, num_experts, topk) and
@@ -215,7 +217,8 @@ moe_status moe_get_workspace(moe_ctx* ctx, moe_workspace_view* out);
 
 /* Synchronise ctx's device, read and clear the device error word.
  * *device_flags receives MOE_DEVERR_* bits. Returns MOE_OK when no bit was
- * set, else MOE_ERR_BAD_EXPERT_ID or MOE_ERR_TIMEOUT (timeout wins). */
+ * set, else MOE_ERR_CUDA (MOE_DEVERR_LAUNCH), MOE_ERR_TIMEOUT or
+ * MOE_ERR_BAD_EXPERT_ID, in that order of precedence. */
 moe_status moe_get_error(moe_ctx* ctx, int32_t* device_flags);
 
 /* Benchmark support: when enabled, each moe_forward records a CUDA event on

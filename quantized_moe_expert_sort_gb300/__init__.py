@@ -204,14 +204,15 @@ class MoE:
         """Copies of the stage-1 output rows of the last forward: (codes, scales, fmt).
 
         fmt 'f16' / 'e4m3' / 'e2m1': codes [rows, I * bytes per element], scales [rows, I/32].
-        fmt 'e4m3_hilo' (bf16 activations on the tensor-core path): codes [rows, 2I] and
-        scales [rows, 2I/32], hi in the first half of each, lo in the second; value = hi + lo.
+        fmt 'e2m1x5' (bf16 activations on the tensor-core path): codes [rows, 5 I/2] and scales
+        [rows, 5 I/32], code term t in bytes [t I/2, (t+1) I/2) and scales [t I/32, (t+1) I/32);
+        value = sum of the five terms.
         """
         v = self.workspace()
-        if v.inter_scale_layout == 2:
-            codes = _view(v.inter_codes, (rows, 2 * self.I), torch.uint8).clone()
-            scales = _view(v.inter_scales, (rows, v.inter_scale_stride), torch.uint8)[:, :2 * self.I // 32].clone()
-            return codes, scales, "e4m3_hilo"
+        if v.inter_scale_layout == 2:  # sub-row r * 5 + t holds code term t of row r
+            codes = _view(v.inter_codes, (rows, 5 * self.I // 2), torch.uint8).clone()
+            scales = _view(v.inter_scales, (rows * 5, v.inter_scale_stride), torch.uint8)[:, :self.I // 32]
+            return codes, scales.reshape(rows, 5 * self.I // 32).clone(), "e2m1x5"
         bpe = {"bf16": 2, "fp8": 1, "fp4": 0.5}[a_dtype]
         fmt = {"bf16": "f16", "fp8": "e4m3", "fp4": "e2m1"}[a_dtype]
         codes = _view(v.inter_codes, (rows, int(self.I * bpe)), torch.uint8).clone()

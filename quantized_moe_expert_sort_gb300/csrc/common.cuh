@@ -27,6 +27,7 @@ enum : int {
   DEV_ERR_BAD_EXPERT = 1,   // a routed expert id was outside [0, E); the pair was dropped
   DEV_ERR_TIMEOUT = 2,      // a bounded wait ran out; the kernel returned early
   DEV_ERR_OVERFLOW = 4,     // sorted rows would exceed the workspace; extra rows dropped
+  DEV_ERR_LAUNCH = 8,       // a kernel got less shared memory than its layout needs; it returned at once
 };
 
 __device__ __forceinline__ void set_error(int* err, int bit) {
@@ -80,6 +81,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   uint32_t h;
   asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(h) : "r"(code & 0xFFu));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// One e2m1 code (low nibble) -> its value as fp32 (exact).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
+  uint32_t h;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h) : "r"(code & 0xFu));
   return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
@@ -173,6 +181,13 @@ __host__ __device__ __forceinline__ int fmt_bytes_per_32(int fmt) { return fmt =
 // mbarrier / TMA (inline PTX). Every wait is bounded: on timeout it records
 // DEV_ERR_TIMEOUT and returns false, so no kernel can spin forever.
 // ---------------------------------------------------------------------------
+// Dynamic shared memory this launch was given (bytes).
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t n;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+  return n;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -191,6 +206,12 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Arrive without release semantics: for barriers that only hand back a buffer
+// whose contents this thread has finished reading (nothing it wrote is published).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.relaxed.cta.shared::cta.b64 st, [%0];\n}" :: "r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

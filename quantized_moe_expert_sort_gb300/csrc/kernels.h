@@ -18,6 +18,7 @@ struct SortOut {
   int32_t* active_experts;  // [E]          experts with count > 0, ascending
   int32_t* meta;            // [META_WORDS] num_blocks, num_active, num_rows
   int32_t* pair_row = nullptr;  // [T*K] (optional) sorted row of each pair, -1 if dropped
+  int4* active_info = nullptr;  // [E]   (optional) {expert, count, first row, 0} of each active expert
 };
 
 constexpr int SORT_SMALL_MAX_PAIRS = 8192;  // single-CTA sort up to this many pairs
@@ -35,22 +36,20 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
 cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t st);
 cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
-// Activation quantisation for the tensor-core path: quantise each token once
-// (xq / xs, row-major), then copy each routed pair's row to its sorted row
-// pair_row[p] of xq_sorted and its e8m0 scales into 512-byte tcgen05.cp chunks
-// per 128-row tile.
-cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
-                                    uint8_t* xq, uint8_t* xs, int xs_stride, uint8_t* xq_sorted, uint8_t* xs_chunks,
-                                    float* acc32, int num_sms, cudaStream_t st);
-
-// Activation quantisation for the few-rows-per-expert tensor-core path: each
-// token's row is quantised once (one thread per 32-block) and written straight
-// to the sorted rows of its routed pairs, codes [rows, row_bytes] and e8m0
-// scales [rows, scale_stride], both row-major. mode SW_A8: e4m3; SW_A4: e2m1;
-// SW_A16: the pair (hi, lo) of e4m3 codes whose sum carries the bf16 value
-// (hi in bytes [0, H) of a row, lo in [H, 2H); scales hi in [0, H/32), lo after).
+// Activation quantisation for the tensor-core paths: each token's row is
+// quantised once (one thread per 32-block) and written straight to the sorted
+// rows of its routed pairs, codes [rows, row_bytes] and e8m0 scales
+// [rows, scale_stride], both row-major. mode SW_A8: e4m3; SW_A4: e2m1;
+// SW_A16: A16_TERMS e2m1 terms whose sum carries the bf16 value, term t of
+// sorted row r stored as sub-row r * A16_TERMS + t (codes [sub-rows, H/2],
+// scales [sub-rows, scale_stride]).
+// scale_stride 0 (SW_A8 / SW_A4 only): scales go to the 512-byte tcgen05.cp
+// chunks of 128-row tiles instead (byte 16*(m%32) + 4*(m/32) + b%4 of chunk
+// (r/128) * H/128 + b/4 for sorted row r, m = r % 128, 32-block b).
+// row_tok / row_w (optional): token and top-k weight of every sorted row.
 cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
-                               uint8_t* scales, int scale_stride, float* acc32, int num_sms, cudaStream_t st);
+                               uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
+                               float* row_w, int num_sms, cudaStream_t st);
 
 // Parameters of the grouped stage kernels (decode family).
 struct StageParams {
@@ -71,6 +70,9 @@ struct StageParams {
   uint8_t* os;        // stage 1: [rows, I/32] scales
   float* acc32;       // stage 2: [T, H]
   const float* topk_w;  // stage 2: [T*K]
+  const int32_t* row_tok;  // few-rows path: token of each sorted row
+  const float* row_w;      // few-rows path: top-k weight of each sorted row
+  const int4* active_info; // few-rows path: {expert, count, first row, 0} per active expert
   int xs_stride;       // bytes per row of the activation-scale array (as)
   int aq_stride;       // bytes per row of the activation-code array (few-rows tensor-core path)
   int os_stride;       // stage 1: bytes per row of the output-scale array (os)
@@ -98,6 +100,7 @@ cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtens
 // tcgen05 family for few routed rows per expert (decode): the weight tile is
 // the M = 128 operand and the expert's routed rows the N <= 64 operand.
 enum { SW_A16 = 0, SW_A8 = 1, SW_A4 = 2 };
+constexpr int A16_TERMS = 5;  // e2m1 code terms carrying one bf16 value (few-rows path)
 cudaError_t swap_set_smem_limits();
 cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               int grid, cudaStream_t st);

@@ -67,7 +67,10 @@ __device__ void sort_scan_and_fill(const int* cnt, int* cursor, int E, int tile_
     so.expert_count[e] = c;
     so.expert_offset[e] = off;
     cursor[e] = off;
-    if (c > 0) so.active_experts[ai++] = e;
+    if (c > 0) {
+      if (so.active_info) so.active_info[ai] = make_int4(e, c, off, 0);
+      so.active_experts[ai++] = e;
+    }
     off += padded;
   }
   if (threadIdx.x == 0) {
@@ -314,47 +317,6 @@ __global__ void __launch_bounds__(256) act_encode_f16_kernel(const __nv_bfloat16
   }
 }
 
-// Copy of the quantised activation rows into sorted order for the tensor-core
-// path: one warp per routed pair p, whose token's row (quantised once per token
-// by act_quant_kernel) goes to sorted row r = pair_row[p] with 16-byte stores;
-// its e8m0 scales go into the tile's 512-byte tcgen05.cp chunks (byte
-// 16*(m%32) + 4*(m/32) + b%4 of chunk b/4, m = r % 128).
-__global__ void __launch_bounds__(256) act_gather_sorted_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs,
-                                                                int xs_stride, long pairs, int K, int nb, int row_bytes,
-                                                                const int32_t* __restrict__ pair_row,
-                                                                uint8_t* __restrict__ xq_sorted,
-                                                                uint8_t* __restrict__ xs_chunks) {
-  const int lane = threadIdx.x & 31;
-  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
-  const int nv = row_bytes / 16;  // 16-byte pieces per row (<= 256 for H <= 4096)
-  for (long pr = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < pairs; pr += nwarps) {
-    const int r = pair_row[pr];
-    if (r < 0) continue;  // dropped pair (warp-uniform)
-    const long t = pr / K;
-    const uint4* src = reinterpret_cast<const uint4*>(xq + t * (long)row_bytes);
-    uint4* dst = reinterpret_cast<uint4*>(xq_sorted + (size_t)r * row_bytes);
-    // all loads first (independent, in flight together), then the stores
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i < nv) v[i] = __ldg(src + lane + 32 * i);
-    // scales: one 32-bit word = 4 consecutive 32-blocks = one chunk's bytes for this row
-    const int nw = nb / 4;
-    uint32_t sw[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (lane + 32 * i < nw) sw[i] = __ldg(reinterpret_cast<const uint32_t*>(xs + t * xs_stride) + lane + 32 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i < nv) dst[lane + 32 * i] = v[i];
-    const int m = r & 127;
-    uint8_t* ch = xs_chunks + (size_t)(r >> 7) * nw * 512 + 16 * (m & 31) + 4 * (m >> 5);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (lane + 32 * i < nw) *reinterpret_cast<uint32_t*>(ch + (size_t)(lane + 32 * i) * 512) = sw[i];
-  }
-}
-
 // Thread-local 1x32 scale: amax -> (e8m0 byte, multiplier 2^-E) with
 // E = floor(log2 amax) - emax clamped to [-127, 127]; amax == 0 -> byte 127, 0.
 __device__ __forceinline__ uint32_t block_scale_of(float amax, int emax, float* mul) {
@@ -369,15 +331,20 @@ __device__ __forceinline__ uint32_t block_scale_of(float amax, int emax, float* 
 }
 
 // Quantise one token's 32-block per thread and write it to the sorted rows of
-// the token's K routed pairs (see launch_act_scatter).
-template <int MODE>
+// the token's K routed pairs (see launch_act_scatter). A16: A16_TERMS e2m1
+// terms per value, term t quantising (MX rule) what terms 0..t-1 left over (in
+// fp32 the residual v - code * 2^E is exact), term t of sorted row r written as
+// sub-row r * A16_TERMS + t.
+template <int MODE, bool CHUNK>
 __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
                                                           const int32_t* __restrict__ pair_row,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                          int sstride, float* __restrict__ acc32) {
+                                                          int sstride, float* __restrict__ acc32,
+                                                          const float* __restrict__ topk_w, int32_t* __restrict__ row_tok,
+                                                          float* __restrict__ row_w) {
   const int nb = H / 32;
   const long total = (long)T * nb;
-  const long row_bytes = MODE == SW_A4 ? H / 2 : (MODE == SW_A16 ? 2L * H : (long)H);
+  const long row_bytes = MODE == SW_A8 ? (long)H : H / 2;  // one (sub-)row
   const long nthreads = (long)gridDim.x * blockDim.x;
   for (long w = (long)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += nthreads) {
     const long t = w / nb;
@@ -394,65 +361,64 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
         v[8 * i + 2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
       }
     }
-    float amax = 0.0f;
+    constexpr int kTerms = MODE == SW_A16 ? A16_TERMS : 1;
+    uint32_t c[kTerms][8];  // codes per term: e4m3 bytes (A8) or e2m1 pairs in c[t][0..3] (A4, A16)
+    uint32_t sc[kTerms];    // e8m0 scale byte per term
 #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    uint32_t c0[8], c1[8];  // codes: MODE A8 / A16-hi in c0, A16-lo in c1, A4 in c0[0..3]
-    uint32_t s0, s1 = 127u;
-    float mul;
-    if (MODE == SW_A4) {
-      s0 = block_scale_of(amax, 2, &mul);
+    for (int tt = 0; tt < kTerms; ++tt) {
+      float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          acc |= cvt_e2m1x2(__fmul_rn(v[8 * i + 2 * k], mul), __fmul_rn(v[8 * i + 2 * k + 1], mul)) << (8 * k);
-        c0[i] = acc;
-      }
-    } else {
-      // A8: the MX rule (emax 8, saturating). A16 hi: emax 7, so that no code saturates.
-      s0 = block_scale_of(amax, MODE == SW_A16 ? 7 : 8, &mul);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        c0[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul), __fmul_rn(v[4 * i + 1], mul)) |
-                (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul), __fmul_rn(v[4 * i + 3], mul)) << 16);
-      if (MODE == SW_A16) {
-        // lo: the exact residual v - hi * 2^E, quantised the same way
-        const float inv = e8m0_to_f32(s0);  // 2^E (codes are 0 for an all-zero block)
-        float rmax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float hv = e4m3_to_f32((c0[i >> 2] >> (8 * (i & 3))) & 0xFFu) * inv;
-          v[i] = v[i] - hv;
-          rmax = fmaxf(rmax, fabsf(v[i]));
-        }
-        float mul1;
-        s1 = block_scale_of(rmax, 7, &mul1);
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      float mul;
+      if (MODE == SW_A8) {
+        sc[tt] = block_scale_of(amax, 8, &mul);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          c1[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul1), __fmul_rn(v[4 * i + 1], mul1)) |
-                  (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul1), __fmul_rn(v[4 * i + 3], mul1)) << 16);
+          c[tt][i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul), __fmul_rn(v[4 * i + 1], mul)) |
+                     (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul), __fmul_rn(v[4 * i + 3], mul)) << 16);
+      } else {
+        sc[tt] = block_scale_of(amax, 2, &mul);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t acc = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            acc |= cvt_e2m1x2(__fmul_rn(v[8 * i + 2 * k], mul), __fmul_rn(v[8 * i + 2 * k + 1], mul)) << (8 * k);
+          c[tt][i] = acc;
+        }
+        if (tt + 1 < kTerms) {
+          // A16: the next term quantises the exact residual of this one
+          const float sv = e8m0_to_f32(sc[tt]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] -= e2m1_to_f32((c[tt][i >> 3] >> (4 * (i & 7))) & 0xFu) * sv;
+        }
       }
     }
     for (int k = 0; k < K; ++k) {
       const int r = __ldg(pair_row + t * K + k);
       if (r < 0) continue;
-      uint8_t* dst = codes + (size_t)r * row_bytes;
-      if (MODE == SW_A4) {
-        *reinterpret_cast<uint4*>(dst + 16 * b) = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-      } else {
-        uint4* d0 = reinterpret_cast<uint4*>(dst + 32 * b);
-        d0[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-        d0[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
-        if (MODE == SW_A16) {
-          uint4* d1 = reinterpret_cast<uint4*>(dst + H + 32 * b);
-          d1[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
-          d1[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
-        }
+      if (row_tok && b == 0) {
+        row_tok[r] = (int32_t)t;
+        row_w[r] = __ldg(topk_w + t * K + k);
       }
-      scales[(size_t)r * sstride + b] = (uint8_t)s0;
-      if (MODE == SW_A16) scales[(size_t)r * sstride + nb + b] = (uint8_t)s1;
+      uint8_t* dst = codes + (size_t)r * kTerms * row_bytes;
+      if (MODE == SW_A8) {
+        uint4* d0 = reinterpret_cast<uint4*>(dst + 32 * b);
+        d0[0] = make_uint4(c[0][0], c[0][1], c[0][2], c[0][3]);
+        d0[1] = make_uint4(c[0][4], c[0][5], c[0][6], c[0][7]);
+      } else {
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt)
+          *reinterpret_cast<uint4*>(dst + (size_t)tt * row_bytes + 16 * b) =
+              make_uint4(c[tt][0], c[tt][1], c[tt][2], c[tt][3]);
+      }
+      if (CHUNK) {  // tcgen05.cp chunks of 128-row tiles (many-rows path)
+        const int m = r & 127;
+        scales[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (m & 31) + 4 * (m >> 5) + (b & 3)] = (uint8_t)sc[0];
+      } else {
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt) scales[((size_t)r * kTerms + tt) * sstride + b] = (uint8_t)sc[tt];
+      }
     }
   }
   if (acc32) {
@@ -542,24 +508,9 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_act_quant_sorted(const void* x, int T, int H, int K, int fmt, const int32_t* pair_row,
-                                    uint8_t* xq, uint8_t* xs, int xs_stride, uint8_t* xq_sorted, uint8_t* xs_chunks,
-                                    float* acc32, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_act_quant(x, T, H, fmt, xq, xs, xs_stride, acc32, num_sms, st);
-  if (e != cudaSuccess) return e;
-  const long pairs = (long)T * K;
-  long blocks = (pairs + 7) / 8;
-  long cap = (long)num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  const int row_bytes = H / 32 * fmt_bytes_per_32(fmt);
-  act_gather_sorted_kernel<<<(int)blocks, 256, 0, st>>>(xq, xs, xs_stride, pairs, K, H / 32, row_bytes, pair_row,
-                                                        xq_sorted, xs_chunks);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
-                               uint8_t* scales, int scale_stride, float* acc32, int num_sms, cudaStream_t st) {
+                               uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
+                               float* row_w, int num_sms, cudaStream_t st) {
   const long work = (long)T * (H / 32);
   long blocks = (work + 127) / 128;
   const long floor_blocks = ((long)T * H / 4 + 127) / 128;  // enough threads to zero acc32 quickly
@@ -568,12 +519,16 @@ cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, con
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (mode == SW_A16)
-    act_scatter_kernel<SW_A16><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
-  else if (mode == SW_A8)
-    act_scatter_kernel<SW_A8><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
-  else
-    act_scatter_kernel<SW_A4><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32);
+  const bool chunk = scale_stride == 0;
+#define MOE_SCATTER(M, C) \
+  act_scatter_kernel<M, C><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32, \
+                                                        topk_w, row_tok, row_w)
+  if (mode == SW_A16) MOE_SCATTER(SW_A16, false);
+  else if (mode == SW_A8 && chunk) MOE_SCATTER(SW_A8, true);
+  else if (mode == SW_A8) MOE_SCATTER(SW_A8, false);
+  else if (chunk) MOE_SCATTER(SW_A4, true);
+  else MOE_SCATTER(SW_A4, false);
+#undef MOE_SCATTER
   return cudaGetLastError();
 }
 

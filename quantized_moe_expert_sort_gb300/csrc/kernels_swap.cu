@@ -15,29 +15,33 @@
 //           16-element group per 16 bytes of shared memory, K tile 128.
 //   SW_A4 : kind::mxf4, A and B packed e2m1 ("Add an opt-in a4w4 SiTUv2 MoE
 //           path..."), scale_vec::2X, K tile 256.
-//   SW_A16: bf16 activations ("Retune Kimi-K3 a16w4 MoE tile geometry"). Each
-//           bf16 value is carried as hi + lo, two e4m3 codes with their own
-//           1x32 e8m0 scales (hi: the block rounded to e4m3 with emax 7, so no
-//           code saturates; lo: the exact residual, rounded the same way); two
-//           MMAs accumulate hi and lo into the same accumulator. hi + lo equals
-//           the bf16 value exactly for elements within 2^12 of their block's
-//           largest magnitude, and within 2^-11 of the block maximum otherwise.
+//   SW_A16: bf16 activations ("Retune Kimi-K3 a16w4 MoE tile geometry"), on
+//           kind::mxf4 like SW_A4: each bf16 value is carried as the sum of
+//           kTerms = 5 e2m1 codes, each term with its own 1x32 e8m0 scale (term
+//           t quantises, by the MX rule, what the earlier terms left over).
+//           The sum reproduces ~99.6% of bf16 values exactly and the rest
+//           within ~3e-6 relative (L2), far inside bf16's own rounding (~2e-3);
+//           the weights stay packed. The terms of sorted row r are stored as
+//           sub-rows r * kTerms + t, so they sit side by side in the N dimension
+//           of one MMA (column n * kTerms + t for item row n) and the weights are
+//           read once; few rows need few columns.
 //
-// Unit of work: (active expert, 128-row weight tile). Stage 1 loads the gate
-// and the up rows of the same 128 intermediate columns j as two A tiles into
-// two accumulators, so TMEM lane j holds g and u of column j for every routed
-// row; the epilogue forms y = act(g, u) and requantises y per 32 along I
-// across the warp's 32 lanes. Stage 2 loads 128 rows of H; lane h adds
-// w * z[h] for each routed row into the fp32 combine buffer (one coalesced
-// 128-byte red per warp and row). Experts with more than kNMax rows are
-// split into several items that stream the weight tile again.
+// Unit of work: (active expert, two 128-row weight tiles). Stage 1 loads the
+// gate and the up rows of the same 128 intermediate columns j as the two A
+// tiles, into two accumulators, so TMEM lane j holds g and u of column j for
+// every routed row; the epilogue forms y = act(g, u) and requantises y per 32
+// along I across the warp's 32 lanes. Stage 2 loads 256 consecutive rows of H;
+// lane h adds w * z[h] for each routed row into the fp32 combine buffer (one
+// coalesced 128-byte red per warp and row). Experts with more than kNMax rows
+// are split into several items that stream the weight tiles again.
 //
-// CTA (one per SM, persistent): warp 0 enumerates items, publishes them in a
-// ring in shared memory and issues TMA for the weight tiles and the routed
-// rows (sorted rows are contiguous per expert: no gather); warp 1 copies the
-// e8m0 scales of both operands with cp.async straight into the tcgen05.cp
-// chunk layout, two stages ahead of its mbarrier arrivals; warp 2 owns TMEM
-// and issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue from
+// CTA (one per SM, persistent): warp 3 enumerates the items (expert ids,
+// counts and offsets fetched 32 units at a time) and publishes them in a ring
+// in shared memory; warp 0 issues TMA for the weight tiles and the routed rows
+// (sorted rows are contiguous per expert: no gather); warp 1 copies the e8m0
+// scales of both operands with cp.async straight into the tcgen05.cp chunk
+// layout, two stages ahead of its mbarrier arrivals; warp 2 owns TMEM and
+// issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue from
 // double-buffered accumulators.
 #include "common.cuh"
 #include "kernels.h"
@@ -49,47 +53,55 @@ namespace {
 constexpr int kThreadsSw = 256;
 constexpr int kEpiWarpsSw = 4;
 constexpr int kTile = 128 * 128;  // one 128-row x 128-byte operand tile
-constexpr int kURing = 4;         // items in flight in the shared-memory ring
-constexpr int kSfLag = 2;         // stages warp 1 runs ahead of its arrivals
+constexpr int kURing = 32;        // items in flight in the shared-memory ring
+constexpr int kSfRing = 8;        // scale-chunk slots (a ring of its own, deeper than the operand ring)
+constexpr int kSfLag = 4;         // stages warp 1's copies run ahead of its arrivals
 
 template <int KIND> struct SwKind;
+// kNMax: routed rows per item; kTerms: code terms per value (B rows = kTerms x rows).
 template <> struct SwKind<SW_A16> {
-  static constexpr int kKTile = 128, kBlocks = 4, kChunks = 1, kNMax = 32;
-  static constexpr bool kHiLo = true, kMxf4 = false;
+  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kNMax = 16, kTerms = A16_TERMS;
+  static constexpr bool kMxf4 = true;
 };
 template <> struct SwKind<SW_A8> {
-  static constexpr int kKTile = 128, kBlocks = 4, kChunks = 1, kNMax = 64;
-  static constexpr bool kHiLo = false, kMxf4 = false;
+  static constexpr int kKTile = 128, kBlocks = 4, kChunks = 1, kNMax = 64, kTerms = 1;
+  static constexpr bool kMxf4 = false;
 };
 template <> struct SwKind<SW_A4> {
-  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kNMax = 64;
-  static constexpr bool kHiLo = false, kMxf4 = true;
+  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kNMax = 64, kTerms = 1;
+  static constexpr bool kMxf4 = true;
 };
 
-template <int STAGE> constexpr int sw_stages() { return STAGE == 1 ? 4 : 6; }
+template <int KIND> constexpr int acc_cols() {  // TMEM columns of one accumulator (largest MMA N)
+  return (SwKind<KIND>::kTerms * SwKind<KIND>::kNMax + 15) / 16 * 16;
+}
+
+// Operand pipeline depth: the unpacked (16U4) weight tiles of kind::mxf8f6f4 take
+// twice the shared memory per HBM byte, so that kind gets one more stage.
+template <int KIND> constexpr int sw_stages() { return SwKind<KIND>::kMxf4 ? 4 : 5; }
 
 struct UItem {
   int e, tile, row0, nrows;  // nrows < 0: end of work
-  int pid[64];
-  float w[64];
 };
 
-template <int STAGE> struct SwLayout {
-  static constexpr int kNS = sw_stages<STAGE>();
-  static constexpr uint32_t a_bytes = (STAGE == 1 ? 2 : 1) * kTile;    // gate + up, or one tile
-  static constexpr uint32_t b_bytes = 64 * 128;                        // kNMax rows (x2 for hi / lo at 32)
-  static constexpr uint32_t sf_bytes = 4 * 1024;                       // sfa gate, sfa up, sfb, sfb lo
+template <int KIND> struct SwLayout {
+  static constexpr int kNS = sw_stages<KIND>();
+  static constexpr uint32_t a_bytes = 2 * kTile;                      // two 128-row weight tiles
+  static constexpr uint32_t b_bytes = acc_cols<KIND>() * 128;          // B rows = terms x routed rows
+  static constexpr uint32_t sf_bytes = 3 * 1024;                       // sfa gate, sfa up, sfb
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kNS * a_bytes;
   static constexpr uint32_t sf = b + kNS * b_bytes;
-  static constexpr uint32_t items = sf + kNS * sf_bytes;
+  static constexpr uint32_t items = sf + kSfRing * sf_bytes;
   static constexpr uint32_t bars = items + kURing * sizeof(UItem);
-  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 2 * kURing + 1) * 8;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 2 * kURing + kSfRing + 1) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;  // + alignment slack
 };
 
 constexpr uint32_t kTmemColsSw = 512;
-constexpr uint32_t kSfColSw = 256;  // scale slots: 32 columns per pipeline slot from here
+// TMEM: accumulators (2 buffers x 2 tiles) from column 0, then the scale slots,
+// 32 columns per operand slot.
+template <int KIND> constexpr uint32_t sf_col0() { return 4 * acc_cols<KIND>(); }
 
 __device__ __forceinline__ void tma_load_2d_sw(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -107,6 +119,21 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// L2 prefetch of a contiguous range (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the outcome is broadcast, and the
+// warp reconverges (memory ordering for the data the barrier guards).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_or_abort(bar, parity, err, abort);
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
 // Byte offset of (row m, block kb % 4) inside a 512-byte scale chunk.
 __device__ __forceinline__ uint32_t sf_off_sw(int m) { return 16u * (m & 31) + 4u * (m >> 5); }
 
@@ -120,9 +147,11 @@ template <int KIND, int STAGE>
 __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p, const __grid_constant__ CUtensorMap tm_w,
                                                                    const __grid_constant__ CUtensorMap tm_x) {
   using KD = SwKind<KIND>;
-  using L = SwLayout<STAGE>;
+  using L = SwLayout<KIND>;
   constexpr int kNS = L::kNS;
   constexpr int NMAX = KD::kNMax;
+  constexpr int kAccCols = acc_cols<KIND>();
+  static_assert(4 * kAccCols + sw_stages<KIND>() * 32 <= 512, "TMEM columns");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
@@ -131,23 +160,30 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
   uint64_t* tempty = tfull + 2;
   uint64_t* ufull = tempty + 2;
   uint64_t* uempty = ufull + kURing;
-  uint64_t* drain = uempty + kURing;
+  uint64_t* sfempty = uempty + kURing;  // scale-ring slot free (MMA commit)
+  uint64_t* drain = sfempty + kSfRing;
   UItem* items = reinterpret_cast<UItem*>(smem + L::items);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
   __shared__ int abort_flag;
 
+  if (dynamic_smem_bytes() < L::total) {  // launched with less shared memory than the layout needs
+    if (threadIdx.x == 0) set_error(p.err, DEV_ERR_LAUNCH);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = p.H, I = p.I, K = p.K;
+  const int H = p.H, I = p.I;
   const int kdim = STAGE == 1 ? H : I;
   const int ktiles = (kdim + KD::kKTile - 1) / KD::kKTile;
   const int nblk_k = kdim / 32;
-  const int ntn = STAGE == 1 ? I / 128 : H / 128;
+  const int ntn = STAGE == 1 ? I / 128 : (H + 255) / 256;  // units per expert
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kEpiWarpsSw); }
-    for (int s = 0; s < kURing; ++s) { mbar_init(&ufull[s], 1); mbar_init(&uempty[s], 2 + kEpiWarpsSw); }
+    // an item is released by the TMA issuer, the scale warp, the MMA issuer and the epilogue warps
+    for (int s = 0; s < kURing; ++s) { mbar_init(&ufull[s], 1); mbar_init(&uempty[s], 3 + kEpiWarpsSw); }
+    for (int s = 0; s < kSfRing; ++s) mbar_init(&sfempty[s], 1);
     mbar_init(drain, 1);
     fence_barrier_init();
   }
@@ -166,93 +202,138 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------- item enumeration + TMA producer -------------------
+  if (warp == 3) {
+    // ------------------------------ item scheduler ------------------------------
+    // Units u = blockIdx.x + k * gridDim.x, unit = (active expert u / ntn, tile u % ntn);
+    // {expert, count, first row} of 32 units are fetched at once, one batch ahead.
+    const int nunits = p.meta[META_NUM_ACTIVE] * ntn;
+    int it = 0;
+    bool done = false;
+    long base = blockIdx.x;
+    long u = base + (long)lane * gridDim.x;
+    int4 info = u < nunits ? p.active_info[u / ntn] : make_int4(-1, 0, 0, 0);
+    while (!done) {
+      const int4 cur = info;
+      const long cbase = base;
+      base += 32L * gridDim.x;
+      u = base + (long)lane * gridDim.x;
+      info = u < nunits ? p.active_info[u / ntn] : make_int4(-1, 0, 0, 0);  // next batch, in flight
+      for (int l = 0; l < 32 && !done; ++l) {
+        const long ul = cbase + (long)l * gridDim.x;
+        const int el = __shfl_sync(0xFFFFFFFFu, cur.x, l);
+        const int cl = __shfl_sync(0xFFFFFFFFu, cur.y, l);
+        const int ol = __shfl_sync(0xFFFFFFFFu, cur.z, l);
+        const bool more = ul < nunits;
+        const int nch = more ? (cl + NMAX - 1) / NMAX : 1;
+        for (int ch = 0; ch < nch; ++ch, ++it) {
+          const int us = it % kURing;
+          if (!warp_wait(&uempty[us], ((it / kURing) & 1) ^ 1, p.err, &abort_flag)) { done = true; break; }
+          if (lane == 0) {
+            UItem* ui = items + us;
+            ui->e = el;
+            ui->tile = more ? (int)(ul % ntn) : 0;
+            ui->row0 = ol + ch * NMAX;
+            ui->nrows = more ? min(NMAX, cl - ch * NMAX) : -1;
+            mbar_arrive(&ufull[us]);
+          }
+          __syncwarp();
+          if (!more) { done = true; break; }
+        }
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    // At the start of each item the weight-scale rows of the next item are
+    // prefetched into L2, ahead of the scale warp's 4-byte copies.
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
       tma_prefetch_desc(&tm_x);
-    }
-    const int nunits = p.meta[META_NUM_ACTIVE] * ntn;
-    uint32_t stage = 0;
-    int it = 0;
-    int u = blockIdx.x;
-    int e_next = u < nunits ? p.active_experts[u / ntn] : -1;
-    bool stop = false;
-    while (!stop) {
-      const bool more = u < nunits;
-      const int e = e_next, tile = more ? u % ntn : 0;
-      const int cnt = more ? p.expert_count[e] : 0;
-      const int off = more ? p.expert_offset[e] : 0;
-      u += gridDim.x;
-      e_next = u < nunits ? p.active_experts[u / ntn] : -1;
-      const int nch = more ? (cnt + NMAX - 1) / NMAX : 1;
-      for (int ch = 0; ch < nch; ++ch, ++it) {
+      const int sb_w = kdim / 32;
+      auto prefetch_scales = [&](int j) {
+        const int un = j % kURing;
+        if (!mbar_wait_or_abort(&ufull[un], (j / kURing) & 1, p.err, &abort_flag)) return;
+        const UItem nx = items[un];
+        if (nx.nrows < 0) return;
+        if (STAGE == 1) {
+          const uint8_t* g = p.wscale + ((size_t)nx.e * 2 * I + (size_t)nx.tile * 128) * sb_w;
+          bulk_prefetch_l2(g, 128u * sb_w);
+          bulk_prefetch_l2(g + (size_t)I * sb_w, 128u * sb_w);
+        } else {
+          const int rows = min(256, H - nx.tile * 256);
+          bulk_prefetch_l2(p.wscale + ((size_t)nx.e * H + (size_t)nx.tile * 256) * sb_w, (uint32_t)rows * sb_w);
+        }
+      };
+      prefetch_scales(0);
+      uint32_t stage = 0;
+      int it = 0;
+      bool ok = true;
+      while (ok) {
         const int us = it % kURing;
-        if (!mbar_wait_or_abort(&uempty[us], ((it / kURing) & 1) ^ 1, p.err, &abort_flag)) { stop = true; break; }
-        UItem* ui = items + us;
-        const int row0 = off + ch * NMAX;
-        const int nrows = more ? min(NMAX, cnt - ch * NMAX) : -1;
-        if (STAGE == 2 && more) {
-          for (int n = lane; n < nrows; n += 32) {
-            const int pid = p.sorted_ids[row0 + n];
-            ui->pid[n] = pid;
-            ui->w[n] = p.topk_w[pid];
+        if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
+        const UItem ui = items[us];
+        mbar_arrive_relaxed(&uempty[us]);
+        ++it;
+        if (ui.nrows < 0) break;
+        prefetch_scales(it);
+        const int nsub = ui.nrows * KD::kTerms;  // B rows: the item's sub-rows
+        const int nbox = (nsub + 15) / 16;
+        const uint32_t btx = (uint32_t)nbox * 16 * 128;
+        for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+          const int slot = stage % kNS;
+          if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
+          uint8_t* sa = smem + L::a + slot * L::a_bytes;
+          uint8_t* sb = smem + L::b + slot * L::b_bytes;
+          mbar_arrive_expect_tx(&full[slot], 2 * w_tile_tx<KIND>() + btx);
+          if (STAGE == 1) {
+            tma_load_4d(sa, &tm_w, ks * 128, ui.tile * 128, 0, ui.e, &full[slot]);
+            tma_load_4d(sa + kTile, &tm_w, ks * 128, ui.tile * 128, 1, ui.e, &full[slot]);
+          } else {  // rows past H (odd H / 128) are filled with zeros
+            tma_load_3d(sa, &tm_w, ks * 128, ui.tile * 256, ui.e, &full[slot]);
+            tma_load_3d(sa + kTile, &tm_w, ks * 128, ui.tile * 256 + 128, ui.e, &full[slot]);
           }
+          // routed rows: contiguous sub-rows [row0 * kTerms, (row0 + nrows) * kTerms), 16-row boxes
+          // (rows past this expert belong to later experts and only fill unused columns)
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d_sw(sb + bx * 16 * 128, &tm_x, ks * 128, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
         }
-        if (lane == 0) { ui->e = e; ui->tile = tile; ui->row0 = row0; ui->nrows = nrows; }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ufull[us]);
-        if (!more) { stop = true; break; }
-        if (lane == 0) {
-          const int nbox = (nrows + 15) / 16;
-          const uint32_t btx = (uint32_t)nbox * 16 * 128 * (KD::kHiLo ? 2 : 1);
-          for (int ks = 0; ks < ktiles; ++ks, ++stage) {
-            const int slot = stage % kNS;
-            if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { stop = true; break; }
-            uint8_t* sa = smem + L::a + slot * L::a_bytes;
-            uint8_t* sb = smem + L::b + slot * L::b_bytes;
-            mbar_arrive_expect_tx(&full[slot], (STAGE == 1 ? 2 : 1) * w_tile_tx<KIND>() + btx);
-            if (STAGE == 1) {
-              tma_load_4d(sa, &tm_w, ks * 128, tile * 128, 0, e, &full[slot]);
-              tma_load_4d(sa + kTile, &tm_w, ks * 128, tile * 128, 1, e, &full[slot]);
-            } else {
-              tma_load_3d(sa, &tm_w, ks * 128, tile * 128, e, &full[slot]);
-            }
-            // routed rows: contiguous sorted rows [row0, row0 + nrows), 16-row boxes
-            // (rows past this expert belong to later experts and only fill unused columns)
-            for (int bx = 0; bx < nbox; ++bx) {
-              tma_load_2d_sw(sb + bx * 16 * 128, &tm_x, ks * 128, row0 + 16 * bx, &full[slot]);
-              if (KD::kHiLo)
-                tma_load_2d_sw(sb + (NMAX + bx * 16) * 128, &tm_x, kdim + ks * 128, row0 + 16 * bx, &full[slot]);
-            }
-          }
-        }
-        stop = __shfl_sync(0xFFFFFFFFu, stop ? 1 : 0, 0) != 0;
-        stage = __shfl_sync(0xFFFFFFFFu, stage, 0);
-        if (stop) break;
       }
     }
   } else if (warp == 1) {
     // ---------- e8m0 scales of both operands into tcgen05.cp chunks ----------
+    // Stage g's chunks go to scale slot g % kSfRing (freed by the MMA of stage
+    // g - kSfRing); warp 1 arrives on the operand slot's full barrier kSfLag stages
+    // later, once its copies have landed, after checking that the operand slot
+    // has been re-armed for that stage.
     const int sb_w = kdim / 32;  // weight-scale bytes per row
     uint32_t stage = 0, pend = 0;
     int it = 0;
-    while (true) {
+    bool ok = true;
+    auto arrive_oldest = [&]() {
+      const uint32_t g = stage - pend;
+      // the operand slot of stage g is in g's phase once the MMA released stage g - kNS
+      ok = ok && warp_wait(&empty[g % kNS], ((g / kNS) & 1) ^ 1, p.err, &abort_flag);
+      mbar_arrive(&full[g % kNS]);
+      --pend;
+    };
+    while (ok) {
       const int us = it % kURing;
-      if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
-      const UItem* ui = items + us;
-      const int e = ui->e, tile = ui->tile, row0 = ui->row0, nrows = ui->nrows;
+      if (!warp_wait(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
+      const UItem ui = items[us];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&uempty[us]);
+      if (lane == 0) mbar_arrive_relaxed(&uempty[us]);
       ++it;
-      if (nrows < 0) break;
-      const uint8_t* wsrc = STAGE == 1 ? p.wscale + ((size_t)e * 2 * I + (size_t)tile * 128) * sb_w
-                                       : p.wscale + ((size_t)e * H + (size_t)tile * 128) * sb_w;
-      bool ok = true;
-      for (int ks = 0; ks < ktiles; ++ks) {
-        const int slot = stage % kNS;
-        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
-        uint8_t* sf = smem + L::sf + slot * L::sf_bytes;  // [sfa gate | sfa up | sfb | sfb lo], 1 KB each
+      if (ui.nrows < 0) break;
+      const int nsub = ui.nrows * KD::kTerms;
+      const size_t sub0 = (size_t)ui.row0 * KD::kTerms;
+      // first row of tile 0; tile 1 is I rows further (up rows) in stage 1, 128 rows in stage 2
+      const uint8_t* wsrc = STAGE == 1 ? p.wscale + ((size_t)ui.e * 2 * I + (size_t)ui.tile * 128) * sb_w
+                                       : p.wscale + ((size_t)ui.e * H + (size_t)ui.tile * 256) * sb_w;
+      const size_t w1 = STAGE == 1 ? (size_t)I : 128;
+      const bool t1 = STAGE == 1 || ui.tile * 256 + 128 < H;  // second tile inside the matrix
+      for (int ks = 0; ks < ktiles && ok; ++ks) {
+        const int fslot = stage % kSfRing;
+        if (!warp_wait(&sfempty[fslot], ((stage / kSfRing) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
+        uint8_t* sf = smem + L::sf + fslot * L::sf_bytes;  // [sfa tile 0 | sfa tile 1 | sfb], 1 KB each
         for (int c = 0; c < KD::kChunks; ++c) {
           const int kb0 = ks * KD::kBlocks + 4 * c;
           if (kb0 < nblk_k) {  // kdim % 128 == 0: a chunk is all in or all out
@@ -260,19 +341,15 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
             for (int i = 0; i < 4; ++i) {
               const int m = 4 * lane + i;
               cp_async4(sf + 512 * c + sf_off_sw(m), wsrc + (size_t)m * sb_w + kb0);
-              if (STAGE == 1) cp_async4(sf + 1024 + 512 * c + sf_off_sw(m), wsrc + ((size_t)I + m) * sb_w + kb0);
+              if (t1) cp_async4(sf + 1024 + 512 * c + sf_off_sw(m), wsrc + (w1 + m) * sb_w + kb0);
             }
-            for (int n = lane; n < nrows; n += 32) {
-              const uint8_t* src = p.as + (size_t)(row0 + n) * p.xs_stride + kb0;
-              cp_async4(sf + 2048 + 512 * c + sf_off_sw(n), src);
-              if (KD::kHiLo) cp_async4(sf + 3072 + 512 * c + sf_off_sw(n), src + nblk_k);
-            }
+            for (int n = lane; n < nsub; n += 32)
+              cp_async4(sf + 2048 + 512 * c + sf_off_sw(n), p.as + (sub0 + n) * p.xs_stride + kb0);
           } else {  // past the end of K: neutral scales (the operands there are zero)
             const uint4 n127 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
             *reinterpret_cast<uint4*>(sf + 512 * c + 16 * lane) = n127;
             *reinterpret_cast<uint4*>(sf + 1024 + 512 * c + 16 * lane) = n127;
             *reinterpret_cast<uint4*>(sf + 2048 + 512 * c + 16 * lane) = n127;
-            *reinterpret_cast<uint4*>(sf + 3072 + 512 * c + 16 * lane) = n127;
           }
         }
         cp_async_commit();
@@ -281,74 +358,75 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         if (pend > kSfLag) {
           cp_async_wait<kSfLag>();
           fence_proxy_async();  // this thread's generic-proxy smem writes -> visible to tcgen05.cp
-          mbar_arrive(&full[(stage - pend) % kNS]);
-          --pend;
+          arrive_oldest();
         }
       }
-      if (!ok) break;
     }
     cp_async_wait<0>();
     fence_proxy_async();
-    while (pend > 0) {
-      mbar_arrive(&full[(stage - pend) % kNS]);
-      --pend;
-    }
+    while (pend > 0 && ok) arrive_oldest();
   } else if (warp == 2) {
     // ------------------------------ MMA issuer ------------------------------
+    // One thread; its instruction stream is on the critical path (a block-scaled
+    // MMA takes ~100 cycles), so descriptors are formed once and advanced by adding
+    // 16-byte-unit offsets to their start-address field, and the ring positions
+    // are counters rather than divisions.
     if (lane == 0) {
-      uint32_t stage = 0;
+      const uint64_t dA0 = tc::sdesc(smem_u32(smem + L::a), 16, 1024, tc::SW_128B);
+      const uint64_t dB0 = tc::sdesc(smem_u32(smem + L::b), 16, 1024, tc::SW_128B);
+      const uint64_t dS0 = tc::sdesc(smem_u32(smem + L::sf), 0, 128, tc::SW_NONE);
+      const uint32_t sf0 = tbase + sf_col0<KIND>();
+      int slot = 0, fslot = 0;
+      uint32_t phase = 0;
       int it = 0;
       while (true) {
         const int us = it % kURing;
         if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
         const int nrows = items[us].nrows;
-        mbar_arrive(&uempty[us]);
+        mbar_arrive_relaxed(&uempty[us]);
         if (nrows < 0) break;
         const int buf = it & 1;
         ++it;
         if (!mbar_wait_or_abort(&tempty[buf], (((it - 1) >> 1) & 1) ^ 1, p.err, &abort_flag)) break;
         tc::fence_after();
-        const int nmma = (nrows + 15) / 16 * 16;
-        const uint32_t dg = tbase + buf * 2 * NMAX;
-        const uint32_t du = dg + NMAX;
+        const int nmma = (nrows * KD::kTerms + 15) / 16 * 16;  // the item's sub-rows
+        const uint32_t id0 = KD::kMxf4 ? tc::idesc_bs(128, nmma, tc::MXF4_E2M1, tc::MXF4_E2M1, 0, 0)
+                                       : tc::idesc_bs(128, nmma, tc::F8F6F4_E2M1, tc::F8F6F4_E4M3, 0, 0);
+        const uint32_t dg = tbase + buf * 2 * kAccCols;
         bool ok = true;
-        for (int ks = 0; ks < ktiles; ++ks, ++stage) {
-          const int slot = stage % kNS;
-          if (!mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag)) { ok = false; break; }
+        for (int ks = 0; ks < ktiles; ++ks) {
+          if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag)) { ok = false; break; }
           tc::fence_after();
-          const uint32_t sfc = tbase + kSfColSw + slot * 32;  // sfa gate +0, sfa up +8, sfb +16, sfb lo +24
-          const uint32_t sfs = smem_u32(smem + L::sf + slot * L::sf_bytes);
+          const uint32_t sfc = sf0 + slot * 32;  // sfa tile 0 +0, sfa tile 1 +8, sfb +16
+          const uint64_t ds = dS0 + (uint64_t)((fslot * L::sf_bytes) >> 4);
+#pragma unroll
           for (int c = 0; c < KD::kChunks; ++c) {
-            tc::cp_32x128b_warpx4(sfc + 4 * c, tc::sdesc(sfs + 512 * c, 0, 128, tc::SW_NONE));
-            if (STAGE == 1) tc::cp_32x128b_warpx4(sfc + 8 + 4 * c, tc::sdesc(sfs + 1024 + 512 * c, 0, 128, tc::SW_NONE));
-            tc::cp_32x128b_warpx4(sfc + 16 + 4 * c, tc::sdesc(sfs + 2048 + 512 * c, 0, 128, tc::SW_NONE));
-            if (KD::kHiLo) tc::cp_32x128b_warpx4(sfc + 24 + 4 * c, tc::sdesc(sfs + 3072 + 512 * c, 0, 128, tc::SW_NONE));
+            tc::cp_32x128b_warpx4(sfc + 4 * c, ds + (512 * c >> 4));
+            tc::cp_32x128b_warpx4(sfc + 8 + 4 * c, ds + ((1024 + 512 * c) >> 4));
+            tc::cp_32x128b_warpx4(sfc + 16 + 4 * c, ds + ((2048 + 512 * c) >> 4));
           }
-          const uint32_t sa = smem_u32(smem + L::a + slot * L::a_bytes);
-          const uint32_t sb = smem_u32(smem + L::b + slot * L::b_bytes);
+          const uint64_t da = dA0 + (uint64_t)((slot * L::a_bytes) >> 4);
+          const uint64_t db = dB0 + (uint64_t)((slot * L::b_bytes) >> 4);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint64_t db = tc::sdesc(sb + 32 * i, 16, 1024, tc::SW_128B);
             const uint32_t acc = (ks > 0 || i > 0) ? 1u : 0u;
 #pragma unroll
-            for (int g = 0; g < (STAGE == 1 ? 2 : 1); ++g) {
-              const uint64_t da = tc::sdesc(sa + g * kTile + 32 * i, 16, 1024, tc::SW_128B);
-              const uint32_t d = g == 0 ? dg : du;
-              const uint32_t sfa = sfc + 8 * g;
-              if (KD::kMxf4) {
-                const uint32_t id = tc::idesc_bs(128, nmma, tc::MXF4_E2M1, tc::MXF4_E2M1, 2 * (i & 1), 2 * (i & 1));
-                tc::mma_mxf4(d, da, db, id, sfa + 4 * (i >> 1), sfc + 16 + 4 * (i >> 1), acc);
+            for (int g = 0; g < 2; ++g) {
+              const uint64_t dai = da + ((g * kTile + 32 * i) >> 4);
+              const uint64_t dbi = db + ((32 * i) >> 4);
+              if (KD::kMxf4) {  // scale_vec::2X: K block pair 2(i&1), 2(i&1)+1 of chunk i/2
+                const uint32_t id = id0 | ((2u * (i & 1)) << 4) | ((2u * (i & 1)) << 29);
+                tc::mma_mxf4(dg + g * kAccCols, dai, dbi, id, sfc + 8 * g + 4 * (i >> 1), sfc + 16 + 4 * (i >> 1), acc);
               } else {
-                const uint32_t id = tc::idesc_bs(128, nmma, tc::F8F6F4_E2M1, tc::F8F6F4_E4M3, i, i);
-                tc::mma_mxf8f6f4(d, da, db, id, sfa, sfc + 16, acc);
-                if (KD::kHiLo) {
-                  const uint64_t dbl = tc::sdesc(sb + NMAX * 128 + 32 * i, 16, 1024, tc::SW_128B);
-                  tc::mma_mxf8f6f4(d, da, dbl, id, sfa, sfc + 24, 1u);
-                }
+                const uint32_t id = id0 | ((uint32_t)i << 4) | ((uint32_t)i << 29);
+                tc::mma_mxf8f6f4(dg + g * kAccCols, dai, dbi, id, sfc + 8 * g, sfc + 16, acc);
               }
             }
           }
           tc::commit(&empty[slot]);
+          tc::commit(&sfempty[fslot]);
+          if (++slot == kNS) { slot = 0; phase ^= 1; }
+          if (++fslot == kSfRing) fslot = 0;
         }
         if (!ok) break;
         tc::commit(&tfull[buf]);
@@ -361,63 +439,90 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    int tok_a = 0, tok_b = 0, nt_a = 0, nt_b = 0;
+    float w_a = 0.0f, w_b = 0.0f, nw_a = 0.0f, nw_b = 0.0f;
     int it = 0;
     while (true) {
       const int us = it % kURing;
-      if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
-      const UItem* ui = items + us;
-      const int tile = ui->tile, row0 = ui->row0, nrows = ui->nrows;
-      if (nrows < 0) break;
+      if (!warp_wait(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
+      const UItem ui = items[us];
+      if (ui.nrows < 0) break;
+      const int nrows = ui.nrows, row0 = ui.row0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&uempty[us]);  // the item is in registers
+      // stage 2: token and top-k weight of the item's rows (lanes n and 32 + n); those of
+      // the next item are fetched now, so their latency hides behind this item's work
+      if (STAGE == 2) {
+        if (it == 0) {
+          tok_a = lane < nrows ? p.row_tok[row0 + lane] : 0;
+          w_a = lane < nrows ? p.row_w[row0 + lane] : 0.0f;
+          tok_b = 32 + lane < nrows ? p.row_tok[row0 + 32 + lane] : 0;
+          w_b = 32 + lane < nrows ? p.row_w[row0 + 32 + lane] : 0.0f;
+        } else {
+          tok_a = nt_a; w_a = nw_a; tok_b = nt_b; w_b = nw_b;
+        }
+        const int un = (it + 1) % kURing;
+        if (!warp_wait(&ufull[un], ((it + 1) / kURing) & 1, p.err, &abort_flag)) break;
+        const UItem nx = items[un];
+        if (nx.nrows > 0) {
+          nt_a = lane < nx.nrows ? p.row_tok[nx.row0 + lane] : 0;
+          nw_a = lane < nx.nrows ? p.row_w[nx.row0 + lane] : 0.0f;
+          nt_b = 32 + lane < nx.nrows ? p.row_tok[nx.row0 + 32 + lane] : 0;
+          nw_b = 32 + lane < nx.nrows ? p.row_w[nx.row0 + 32 + lane] : 0.0f;
+        }
+      }
       const int buf = it & 1;
-      if (!mbar_wait_or_abort(&tfull[buf], (it >> 1) & 1, p.err, &abort_flag)) break;
-      ++it;
-      __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+      if (!warp_wait(&tfull[buf], (it >> 1) & 1, p.err, &abort_flag)) break;
+      ++it;  // (warp_wait reconverged the warp: tcgen05.ld is .sync.aligned)
       tc::fence_after();
-      const uint32_t dg = tbase + lane_off + buf * 2 * NMAX;
+      const uint32_t dg = tbase + lane_off + buf * 2 * kAccCols;
+      // Values of item rows [c0, c0 + 16) of one accumulator: row n sums columns
+      // n * kTerms + t (its code terms); only the chunks of 16 columns in use are read.
+      auto load_cols = [&](uint32_t acc, int c0, float* v) {
+        constexpr int kCh = KD::kTerms;  // 16 rows x kTerms columns = kTerms chunks of 16
+        uint32_t r[kCh][16];
+        const int nch = (min(16, nrows - c0) * KD::kTerms + 15) / 16;
+#pragma unroll
+        for (int ch = 0; ch < kCh; ++ch)
+          if (ch < nch) tc::ld_32x32b_x16(acc + c0 * KD::kTerms + 16 * ch, r[ch]);
+        tc::ld_wait();
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          float a = 0.0f;
+#pragma unroll
+          for (int t = 0; t < KD::kTerms; ++t) {
+            const int col = n * KD::kTerms + t;
+            if (col / 16 < nch) a += __uint_as_float(r[col / 16][col % 16]);
+          }
+          v[n] = a;
+        }
+      };
+      // after the item's last TMEM load the accumulator goes back to the MMA warp,
+      // before this item's global stores (so the release does not wait for them)
+      auto release_acc = [&](int c0) {
+        if (c0 + 16 >= nrows) {
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+      };
       if (STAGE == 1) {
-        const int j = tile * 128 + 32 * q + lane;  // intermediate column of this lane
+        const int j = ui.tile * 128 + 32 * q + lane;  // intermediate column of this lane
         for (int c0 = 0; c0 < nrows; c0 += 16) {
-          uint32_t gr[16], ur[16];
-          tc::ld_32x32b_x16(dg + c0, gr);
-          tc::ld_32x32b_x16(dg + NMAX + c0, ur);
-          tc::ld_wait();
+          float gv[16], uv[16];
+          load_cols(dg, c0, gv);
+          load_cols(dg + kAccCols, c0, uv);
+          release_acc(c0);
           const int nn = min(16, nrows - c0);
 #pragma unroll
           for (int n = 0; n < 16; ++n) {
             if (n < nn) {
               const int row = row0 + c0 + n;
-              float y = act_apply(p.act, __uint_as_float(gr[n]), __uint_as_float(ur[n]), p.beta, p.lbeta);
-              if (KD::kHiLo) {
-                // bf16 intermediate, carried as hi + lo e4m3 (same rule as the activations)
-                y = __bfloat162float(__float2bfloat16_rn(y));
-                const float amax = warp_max(fabsf(y));
-                uint32_t s0 = 127u;
-                float mul = 0.0f;
-                if (amax > 0.0f) {
-                  int E = floor_log2_f32(amax) - 7;
-                  E = E < -127 ? -127 : (E > 127 ? 127 : E);
-                  s0 = (uint32_t)(E + 127);
-                  mul = exp2_neg(E);
-                }
-                const uint32_t hc = cvt_e4m3x2(__fmul_rn(y, mul), 0.0f) & 0xFFu;
-                const float r = y - e4m3_to_f32(hc) * e8m0_to_f32(s0);
-                const float rmax = warp_max(fabsf(r));
-                uint32_t s1 = 127u;
-                float mul1 = 0.0f;
-                if (rmax > 0.0f) {
-                  int E = floor_log2_f32(rmax) - 7;
-                  E = E < -127 ? -127 : (E > 127 ? 127 : E);
-                  s1 = (uint32_t)(E + 127);
-                  mul1 = exp2_neg(E);
-                }
-                const uint32_t lc = cvt_e4m3x2(__fmul_rn(r, mul1), 0.0f) & 0xFFu;
-                p.oq[(size_t)row * (2 * I) + j] = (uint8_t)hc;
-                p.oq[(size_t)row * (2 * I) + I + j] = (uint8_t)lc;
-                if (lane == 0) {
-                  p.os[(size_t)row * p.os_stride + j / 32] = (uint8_t)s0;
-                  p.os[(size_t)row * p.os_stride + I / 32 + j / 32] = (uint8_t)s1;
-                }
-              } else {
+              float y = act_apply(p.act, gv[n], uv[n], p.beta, p.lbeta);
+              // A16: the bf16 intermediate; each code term quantises what the earlier ones left
+              if (KD::kTerms > 1) y = __bfloat162float(__float2bfloat16_rn(y));
+#pragma unroll
+              for (int t = 0; t < KD::kTerms; ++t) {
                 const int emax = KD::kMxf4 ? 2 : 8;
                 const float amax = warp_max(fabsf(y));
                 uint32_t sb = 127u;
@@ -431,37 +536,38 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
                 if (KD::kMxf4) {
                   const uint32_t code = cvt_e2m1x2(__fmul_rn(y, mul), 0.0f) & 0xFu;
                   const uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                  if ((lane & 1) == 0) p.oq[(size_t)row * (I / 2) + j / 2] = (uint8_t)(code | (nb << 4));
+                  if ((lane & 1) == 0)
+                    p.oq[((size_t)row * KD::kTerms + t) * (I / 2) + j / 2] = (uint8_t)(code | (nb << 4));
+                  if (t + 1 < KD::kTerms) y -= e2m1_to_f32(code) * e8m0_to_f32(sb);  // exact residual
                 } else {
                   p.oq[(size_t)row * I + j] = (uint8_t)(cvt_e4m3x2(__fmul_rn(y, mul), 0.0f) & 0xFFu);
                 }
-                if (lane == 0) p.os[(size_t)row * p.os_stride + j / 32] = (uint8_t)sb;
+                if (lane == 0) p.os[((size_t)row * KD::kTerms + t) * p.os_stride + j / 32] = (uint8_t)sb;
               }
             }
           }
         }
       } else {
-        const int h = tile * 128 + 32 * q + lane;
+        const int h0 = ui.tile * 256 + 32 * q + lane;  // rows of H of this lane in tiles 0 and 1
+        const bool h1ok = h0 + 128 < H;
         for (int c0 = 0; c0 < nrows; c0 += 16) {
-          uint32_t r[16];
-          tc::ld_32x32b_x16(dg + c0, r);
-          tc::ld_wait();
+          float v0[16], v1[16];
+          load_cols(dg, c0, v0);
+          load_cols(dg + kAccCols, c0, v1);
+          release_acc(c0);
           const int nn = min(16, nrows - c0);
 #pragma unroll
           for (int n = 0; n < 16; ++n) {
             if (n < nn) {
-              const int pid = ui->pid[c0 + n];
-              const float w = ui->w[c0 + n];
-              atomicAdd(p.acc32 + (size_t)(pid / K) * H + h, w * __uint_as_float(r[n]));
+              const int col = c0 + n;  // warp-uniform
+              const int t = __shfl_sync(0xFFFFFFFFu, col < 32 ? tok_a : tok_b, col & 31);
+              const float w = __shfl_sync(0xFFFFFFFFu, col < 32 ? w_a : w_b, col & 31);
+              float* dst = p.acc32 + (size_t)t * H + h0;
+              atomicAdd(dst, w * v0[n]);
+              if (h1ok) atomicAdd(dst + 128, w * v1[n]);
             }
           }
         }
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&tempty[buf]);
-        mbar_arrive(&uempty[us]);
       }
     }
   }
@@ -478,7 +584,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
 template <int KIND, int STAGE>
 static cudaError_t set_limit_sw() {
   return cudaFuncSetAttribute(swap_stage_kernel<KIND, STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)SwLayout<STAGE>::total);
+                              (int)SwLayout<KIND>::total);
 }
 
 cudaError_t swap_set_smem_limits() {
@@ -495,9 +601,9 @@ template <int KIND>
 static void launch_sw(int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x, int grid,
                       cudaStream_t st) {
   if (stage == 1)
-    swap_stage_kernel<KIND, 1><<<grid, kThreadsSw, SwLayout<1>::total, st>>>(p, tm_w, tm_x);
+    swap_stage_kernel<KIND, 1><<<grid, kThreadsSw, SwLayout<KIND>::total, st>>>(p, tm_w, tm_x);
   else
-    swap_stage_kernel<KIND, 2><<<grid, kThreadsSw, SwLayout<2>::total, st>>>(p, tm_w, tm_x);
+    swap_stage_kernel<KIND, 2><<<grid, kThreadsSw, SwLayout<KIND>::total, st>>>(p, tm_w, tm_x);
 }
 
 cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,

@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   __shared__ int abort_flag;
   __shared__ __align__(8) uint64_t drain;  // completion of every tcgen05 op of the MMA thread
 
+  if (dynamic_smem_bytes() < TcLayout::total) {  // launched with less shared memory than the layout needs
+    if (threadIdx.x == 0) set_error(p.err, DEV_ERR_LAUNCH);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, I = p.I, K = p.K, T = p.T;
   const long TK = (long)T * K;
@@ -230,7 +234,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
     }
   } else if (warp == 2) {
     // ------------------------------ MMA issuer ------------------------------
+    // Descriptors are formed once and advanced by 16-byte-unit offsets (the
+    // issuing thread's instruction stream is on the critical path).
     if (lane == 0) {
+      const uint64_t dA0 = tc::sdesc(smem_u32(smem + TcLayout::a), 16, 1024, tc::SW_128B);
+      const uint64_t dB0 = tc::sdesc(smem_u32(smem + TcLayout::b), 16, 1024, tc::SW_128B);
+      const uint64_t dSA = tc::sdesc(smem_u32(smem + TcLayout::sfa), 0, 128, tc::SW_NONE);
+      const uint64_t dSB = tc::sdesc(smem_u32(smem + TcLayout::sfb), 0, 128, tc::SW_NONE);
+      constexpr uint32_t id0 = KIND == TC_A8W4 ? tc::idesc_bs(kBM, kBN, tc::F8F6F4_E4M3, tc::F8F6F4_E2M1, 0, 0)
+                                               : tc::idesc_bs(kBM, kBN, tc::MXF4_E2M1, tc::MXF4_E2M1, 0, 0);
       uint32_t stage = 0;
       int lt = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
@@ -244,22 +256,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           tc::fence_after();
           const uint32_t sfa = tbase + kSfCol0 + slot * 16;
           const uint32_t sfb = sfa + 8;
+#pragma unroll
           for (int c = 0; c < KD::kChunks; ++c) {
-            tc::cp_32x128b_warpx4(sfa + 4 * c, tc::sdesc(smem_u32(smem + TcLayout::sfa + slot * 1024 + 512 * c), 0, 128, tc::SW_NONE));
-            tc::cp_32x128b_warpx4(sfb + 4 * c, tc::sdesc(smem_u32(smem + TcLayout::sfb + slot * 1024 + 512 * c), 0, 128, tc::SW_NONE));
+            tc::cp_32x128b_warpx4(sfa + 4 * c, dSA + ((slot * 1024 + 512 * c) >> 4));
+            tc::cp_32x128b_warpx4(sfb + 4 * c, dSB + ((slot * 1024 + 512 * c) >> 4));
           }
-          const uint32_t sa = smem_u32(smem + TcLayout::a + slot * kTileBytes);
-          const uint32_t sb = smem_u32(smem + TcLayout::b + slot * kTileBytes);
+          const uint64_t da = dA0 + ((slot * kTileBytes) >> 4);
+          const uint64_t db = dB0 + ((slot * kTileBytes) >> 4);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint64_t da = tc::sdesc(sa + 32 * i, 16, 1024, tc::SW_128B);
-            const uint64_t db = tc::sdesc(sb + 32 * i, 16, 1024, tc::SW_128B);
             const uint32_t acc = (ks > 0 || i > 0) ? 1u : 0u;
             if (KIND == TC_A8W4) {
-              tc::mma_mxf8f6f4(d, da, db, tc::idesc_bs(kBM, kBN, tc::F8F6F4_E4M3, tc::F8F6F4_E2M1, i, i), sfa, sfb, acc);
+              tc::mma_mxf8f6f4(d, da + 2 * i, db + 2 * i, id0 | ((uint32_t)i << 4) | ((uint32_t)i << 29), sfa, sfb, acc);
             } else {
-              const uint32_t id = tc::idesc_bs(kBM, kBN, tc::MXF4_E2M1, tc::MXF4_E2M1, 2 * (i & 1), 2 * (i & 1));
-              tc::mma_mxf4(d, da, db, id, sfa + 4 * (i >> 1), sfb + 4 * (i >> 1), acc);
+              const uint32_t id = id0 | ((2u * (i & 1)) << 4) | ((2u * (i & 1)) << 29);
+              tc::mma_mxf4(d, da + 2 * i, db + 2 * i, id, sfa + 4 * (i >> 1), sfb + 4 * (i >> 1), acc);
             }
           }
           tc::commit(&empty[slot]);
@@ -296,6 +307,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           tc::ld_32x32b_x16(d + 64 + 32 * h, ur);
           tc::ld_32x32b_x16(d + 64 + 32 * h + 16, ur + 16);
           tc::ld_wait();
+          // the accumulator goes back to the MMA warp before this tile's global stores
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
           float y[32];
           float amax = 0.0f;
 #pragma unroll
@@ -354,12 +369,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         const float wt = valid ? p.topk_w[pid] : 0.0f;
         float* tb = reinterpret_cast<float*>(smem + TcLayout::epi + (warp - 4) * TcLayout::epi_bytes);
         const unsigned vmask = __ballot_sync(0xFFFFFFFFu, valid);
-#pragma unroll 1
-        for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
-          uint32_t r[32];
-          tc::ld_32x32b_x16(d + 32 * c, r);
-          tc::ld_32x32b_x16(d + 32 * c + 16, r + 16);
-          tc::ld_wait();
+        uint32_t rr2[2][32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          tc::ld_32x32b_x16(d + 32 * (2 * grp + cc), rr2[cc]);
+          tc::ld_32x32b_x16(d + 32 * (2 * grp + cc) + 16, rr2[cc] + 16);
+        }
+        tc::ld_wait();
+        // the accumulator goes back to the MMA warp before this tile's reductions
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * grp + cc;
+          const uint32_t* r = rr2[cc];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             *reinterpret_cast<float4*>(tb + lane * 36 + 4 * i) =
@@ -378,9 +402,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           __syncwarp();
         }
       }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
   tc::fence_before();

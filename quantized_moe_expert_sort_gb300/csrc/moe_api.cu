@@ -71,6 +71,9 @@ struct moe_ctx {
   uint8_t *xq, *xs, *inter_q, *inter_s;
   uint8_t *xq_sorted, *xs_sorted;  // tensor-core path: activations in sorted order + chunked scales
   int32_t* pair_row;
+  int32_t* row_tok;  // few-rows path: token and top-k weight of every sorted row
+  float* row_w;
+  int4* active_info;
   float* acc32;
   int* err;
   void* st_x;
@@ -108,7 +111,7 @@ static void prof_mark(moe_ctx* c, cudaStream_t st, const char* name) {
 static void free_ctx(moe_ctx* c) {
   void* ptrs[] = {c->sorted_ids, c->block_expert, c->expert_count, c->expert_offset, c->active_experts,
                   c->meta, c->hist, c->xq, c->xs, c->inter_q, c->inter_s, c->acc32, c->err,
-                  c->xq_sorted, c->xs_sorted, c->pair_row,
+                  c->xq_sorted, c->xs_sorted, c->pair_row, c->row_tok, c->row_w, c->active_info,
                   c->st_x, c->st_ids, c->st_w, c->st_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -302,12 +305,15 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->hist, sizeof(int32_t) * (size_t)c->hist_chunks * E},
       {(void**)&c->xq, (size_t)max_tokens * H * 2},
       {(void**)&c->xs, (size_t)max_tokens * scale_row_stride(H)},
-      {(void**)&c->inter_q, (size_t)c->cap_rows * I * 2},
-      {(void**)&c->inter_s, (size_t)c->cap_rows * scale_row_stride(2 * I)},
+      {(void**)&c->inter_q, (size_t)c->cap_rows * (A16_TERMS * I / 2 > 2 * I ? A16_TERMS * I / 2 : 2 * I)},
+      {(void**)&c->inter_s, (size_t)c->cap_rows * A16_TERMS * scale_row_stride(I)},
       {(void**)&c->acc32, sizeof(float) * (size_t)max_tokens * H},
-      {(void**)&c->xq_sorted, (size_t)c->cap_rows * H * 2},
-      {(void**)&c->xs_sorted, (size_t)c->cap_rows * scale_row_stride(2 * H)},
+      {(void**)&c->xq_sorted, (size_t)c->cap_rows * A16_TERMS * H / 2},
+      {(void**)&c->xs_sorted, (size_t)c->cap_rows * A16_TERMS * scale_row_stride(H)},
       {(void**)&c->pair_row, sizeof(int32_t) * pairs},
+      {(void**)&c->row_tok, sizeof(int32_t) * c->cap_rows},
+      {(void**)&c->row_w, sizeof(float) * c->cap_rows},
+      {(void**)&c->active_info, sizeof(int4) * E},
       {(void**)&c->err, sizeof(int) * 4},
       {(void**)&c->st_x, (size_t)max_tokens * H * 2},
       {(void**)&c->st_ids, sizeof(int32_t) * pairs},
@@ -412,12 +418,14 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   const int tile_m = use_tc ? TC_TILE_M : (use_sw ? 1 : kDecodeTile);
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
   const int swkind = adt == MOE_A_BF16 ? SW_A16 : (adt == MOE_A_FP8 ? SW_A8 : SW_A4);
-  const int wkind = adt == MOE_A_FP4 ? TC_A4W4 : TC_A8W4;  // weight map type: packed for mxf4, unpacked otherwise
-  // few-rows path: row bytes of the sorted activations / intermediate and their scale strides
-  const int x_row = adt == MOE_A_BF16 ? 2 * c->H : (adt == MOE_A_FP8 ? c->H : c->H / 2);
-  const int i_row = adt == MOE_A_BF16 ? 2 * c->I : (adt == MOE_A_FP8 ? c->I : c->I / 2);
-  const int xs_sw = scale_row_stride(adt == MOE_A_BF16 ? 2 * c->H : c->H);
-  const int is_sw = scale_row_stride(adt == MOE_A_BF16 ? 2 * c->I : c->I);
+  const int wkind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;  // weight map type: unpacked for mxf8f6f4, packed for mxf4
+  // few-rows path: sub-rows per sorted row (bf16: A16_TERMS e2m1 code terms), bytes per
+  // sub-row of the sorted activations / intermediate, and their scale strides
+  const int subs = adt == MOE_A_BF16 ? A16_TERMS : 1;
+  const int x_row = adt == MOE_A_FP8 ? c->H : c->H / 2;
+  const int i_row = adt == MOE_A_FP8 ? c->I : c->I / 2;
+  const int xs_sw = scale_row_stride(c->H);
+  const int is_sw = scale_row_stride(c->I);
   CUtensorMap tm_inter, tm_xs;
   moe_status ms;
   if (use_tc) {
@@ -440,10 +448,10 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     ms = make_w2tc_map(c, w2, wkind);
     if (ms != MOE_OK) return ms;
     cuuint32_t box[2] = {128, 16};
-    cuuint64_t idims[2] = {(cuuint64_t)i_row, (cuuint64_t)c->cap_rows}, istr[1] = {(cuuint64_t)i_row};
+    cuuint64_t idims[2] = {(cuuint64_t)i_row, (cuuint64_t)c->cap_rows * subs}, istr[1] = {(cuuint64_t)i_row};
     ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, box, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate rows");
     if (ms != MOE_OK) return ms;
-    cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows}, xstr[1] = {(cuuint64_t)x_row};
+    cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows * subs}, xstr[1] = {(cuuint64_t)x_row};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, box, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activation rows");
     if (ms != MOE_OK) return ms;
   } else {
@@ -457,6 +465,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   prof_mark(c, st, "sort");
   SortOut so = sort_out(c);
   if (use_tc || use_sw) so.pair_row = c->pair_row;
+  if (use_sw) so.active_info = c->active_info;
   cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
   if (e != cudaSuccess) return cuda_fail(e, "sort launch");
   c->last_tile_m = tile_m;
@@ -464,11 +473,11 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   c->last_inter_stride = use_sw ? is_sw : scale_row_stride(c->I);
   prof_mark(c, st, "act_quant");
   if (use_tc)
-    e = launch_act_quant_sorted(x, T, c->H, c->K, fmt, c->pair_row, c->xq, c->xs, scale_row_stride(c->H), c->xq_sorted,
-                                c->xs_sorted, c->acc32, c->num_sms, st);
+    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, 0, c->acc32, nullptr,
+                           nullptr, nullptr, c->num_sms, st);
   else if (use_sw)
-    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, xs_sw, c->acc32,
-                           c->num_sms, st);
+    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, xs_sw, c->acc32, w,
+                           c->row_tok, c->row_w, c->num_sms, st);
   else
     e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
@@ -479,6 +488,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   p.expert_offset = c->expert_offset;
   p.expert_count = c->expert_count;
   p.active_experts = c->active_experts;
+  p.active_info = c->active_info;
   p.meta = c->meta;
   p.T = T; p.H = c->H; p.I = c->I; p.E = c->E; p.K = c->K;
   p.act = act; p.beta = beta; p.lbeta = lbeta;
@@ -507,7 +517,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   } else if (use_sw) {
-    const long u1 = max_active * (c->I / 128), u2 = max_active * (c->H / 128);
+    const long u1 = max_active * (c->I / 128), u2 = max_active * ((c->H + 255) / 256);
     StageParams q1 = p1;
     q1.aq = c->xq_sorted;
     q1.as = c->xs_sorted;
@@ -518,6 +528,8 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     StageParams q2 = p2;
     q2.xs_stride = is_sw;
+    q2.row_tok = c->row_tok;
+    q2.row_w = c->row_w;
     prof_mark(c, st, "stage2");
     e = launch_swap_stage(swkind, 2, q2, c->tm_w2tc, tm_inter, (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
@@ -622,6 +634,7 @@ moe_status moe_get_error(moe_ctx* c, int32_t* flags) {
   CUDA_TRY(cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
   if (flags) *flags = v;
+  if (v & DEV_ERR_LAUNCH) return fail(MOE_ERR_CUDA, "a kernel was launched with too little shared memory");
   if (v & DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
   if (v & DEV_ERR_BAD_EXPERT) return MOE_ERR_BAD_EXPERT_ID;
   return MOE_OK;

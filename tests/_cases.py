@@ -72,10 +72,10 @@ def to_dev(case, device="cuda"):
 
 def decode_intermediate(codes, scales, fmt):
     """Decode the (codes, scales, fmt) triple of MoE.intermediate() to float64."""
-    if fmt == "e4m3_hilo":
-        I = codes.shape[1] // 2
-        v = decode_codes(codes, scales, "fp8")
-        return v[:, :I] + v[:, I:]
+    if fmt.startswith("e2m1x"):  # a sum of e2m1 code terms
+        n = int(fmt[5:])
+        hb, nb = codes.shape[1] // n, scales.shape[1] // n
+        return sum(decode_codes(codes[:, t * hb:(t + 1) * hb], scales[:, t * nb:(t + 1) * nb], "fp4") for t in range(n))
     return decode_codes(codes, scales, {"f16": "bf16", "e4m3": "fp8", "e2m1": "fp4"}[fmt])
 
 

@@ -134,7 +134,10 @@ def test_tiny_forward(act, a_dtype):
     want = inter[sid[valid]]
     assert rel_l2(got, want) <= TOL
     if a_dtype == "bf16":
-        assert np.mean(got == want) > 0.97  # same bf16 rounding except at near-ties
+        # the bf16 intermediate is carried as five e2m1 code terms: almost all values
+        # exactly, the rest far inside bf16's own rounding error (about 2e-3 relative)
+        assert rel_l2(got, want) <= 1e-4
+        assert np.mean(got == want) > 0.95
 
 
 @pytest.mark.parametrize("T", [1, 4, 16, 64])
