@@ -77,37 +77,11 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return (uint32_t)out;
 }
 
-// One e4m3 code (low byte) -> its value as fp32 (exact).
-__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
-  uint32_t h;
-  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(h) : "r"(code & 0xFFu));
-  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-}
-
 // One e2m1 code (low nibble) -> its value as fp32 (exact).
 __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
   uint32_t h;
   asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h) : "r"(code & 0xFu));
   return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-}
-
-// Eight e2m1 codes (nibble i = element i) -> four f16x2 words; word j holds
-// elements 2j (low half) and 2j+1 (high half).
-__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
-}
-
-// Eight e2m1 codes (nibble i = element i) -> eight e4m3 bytes holding
-// 2^-6 * value, split into even and odd elements:
-//   even byte j = element 2j, odd byte j = element 2j+1.
-// e2m1 s.e1e0.m maps to e4m3 s.00e1e0.m00 (exponent field e1e0, top mantissa
-// bit m), whose value is exactly 2^-6 times the e2m1 value, subnormals included.
-__device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t w, uint32_t& even, uint32_t& odd) {
-  even = ((w << 2) & 0x1C1C1C1Cu) | ((w << 4) & 0x80808080u);
-  odd = ((w >> 2) & 0x1C1C1C1Cu) | (w & 0x80808080u);
 }
 
 // ---------------------------------------------------------------------------
@@ -276,32 +250,5 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, int
                : "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// Register-operand MMA (m16n8, fp32 accumulate)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_e4m3_16832(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Swizzled byte offset inside a TMA tile whose rows are `row_bytes` long
-// (64 -> SWIZZLE_64B, 128 -> SWIZZLE_128B): the 16-byte chunk index is
-// XOR-ed with bits [7, 7+log2(row_bytes/16)) of the row's byte address.
-__device__ __forceinline__ uint32_t swz_offset(uint32_t row, uint32_t chunk, uint32_t row_bytes) {
-  uint32_t addr = row * row_bytes;
-  uint32_t mask = row_bytes / 16 - 1;
-  return addr + (((chunk ^ (addr >> 7)) & mask) << 4);
-}
 
 }  // namespace moe

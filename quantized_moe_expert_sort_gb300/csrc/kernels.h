@@ -51,7 +51,7 @@ cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, con
                                uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
                                float* row_w, int num_sms, cudaStream_t st);
 
-// Parameters of the grouped stage kernels (decode family).
+// Parameters of the grouped stage kernels.
 struct StageParams {
   // activation operand of this stage: block-scaled codes [rows, Kdim] + e8m0 [rows, Kdim/32]
   const uint8_t* aq;
@@ -82,8 +82,6 @@ struct StageParams {
   int* err;
 };
 
-constexpr int DEC_TOK = 8;       // tokens per MMA column group (mma n8)
-
 // Row stride of the workspace's e8m0 scale arrays: kdim/32 bytes rounded up to
 // 16, so that every row can be moved with one 16-byte-aligned bulk copy.
 __host__ __device__ inline int scale_row_stride(int kdim) { return ((kdim / 32) + 15) & ~15; }
@@ -105,10 +103,5 @@ cudaError_t swap_set_smem_limits();
 cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               int grid, cudaStream_t st);
 
-cudaError_t decode_set_smem_limits();
-int decode_s1_blocks_per_sm(int fmt, int H);
-int decode_s2_blocks_per_sm(int fmt, int I);
-cudaError_t launch_decode_stage1(int fmt, const StageParams& p, const CUtensorMap& tm_w13, int grid, cudaStream_t st);
-cudaError_t launch_decode_stage2(int fmt, const StageParams& p, const CUtensorMap& tm_w2, int grid, cudaStream_t st);
 
 }  // namespace moe

@@ -35,7 +35,6 @@ moe_status cuda_fail(cudaError_t e, const char* what) {
   } while (0)
 
 constexpr int kMaxTile = 256;       // largest tile_m the sort accepts
-constexpr int kDecodeTile = DEC_TOK;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -80,16 +79,10 @@ struct moe_ctx {
   int32_t* st_ids;
   float* st_w;
   void* st_out;
-  int s1_bps[3], s2_bps[3];
-  const void* tm_w13_key;
-  CUtensorMap tm_w13;
-  const void* tm_w2_key;
-  CUtensorMap tm_w2;
   // tcgen05 family maps (keyed by pointer and kind)
   const void* tm_w13tc_key; int tm_w13tc_kind; CUtensorMap tm_w13tc;
   const void* tm_w2tc_key; int tm_w2tc_kind; CUtensorMap tm_w2tc;
   const void* tm_w13sw_key; int tm_w13sw_kind; CUtensorMap tm_w13sw;  // 128-row gate / up tiles
-  int legacy_decode;  // MOE_DECODE_LEGACY=1: register-dequantising decode kernels for few rows per expert
   int last_inter_stride;
   int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
   int last_inter_layout;
@@ -118,38 +111,6 @@ static void free_ctx(moe_ctx* c) {
   for (cudaEvent_t e : c->ev)
     if (e) cudaEventDestroy(e);
   delete c;
-}
-
-static moe_status make_w13_map(moe_ctx* c, const uint8_t* w13) {
-  if (c->tm_w13_key == w13) return MOE_OK;
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  cuuint64_t dims[4] = {(cuuint64_t)c->H / 2, (cuuint64_t)c->I, 2, (cuuint64_t)c->E};
-  cuuint64_t strides[3] = {(cuuint64_t)c->H / 2, (cuuint64_t)c->I * c->H / 2, (cuuint64_t)2 * c->I * c->H / 2};
-  cuuint32_t box[4] = {64, 32, 2, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(&c->tm_w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(w13), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(w13) failed: %d", (int)r);
-  c->tm_w13_key = w13;
-  return MOE_OK;
-}
-
-static moe_status make_w2_map(moe_ctx* c, const uint8_t* w2) {
-  if (c->tm_w2_key == w2) return MOE_OK;
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  cuuint64_t dims[3] = {(cuuint64_t)c->I / 2, (cuuint64_t)c->H, (cuuint64_t)c->E};
-  cuuint64_t strides[2] = {(cuuint64_t)c->I / 2, (cuuint64_t)c->H * c->I / 2};
-  cuuint32_t box[3] = {64, 64, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(&c->tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(w2), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(w2) failed: %d", (int)r);
-  c->tm_w2_key = w2;
-  return MOE_OK;
 }
 
 static moe_status encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
@@ -331,7 +292,6 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   cudaError_t e = cudaMemset(c->err, 0, sizeof(int) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->meta, 0, sizeof(int32_t) * META_WORDS);
   if (e == cudaSuccess) e = prep_set_smem_limits();
-  if (e == cudaSuccess) e = decode_set_smem_limits();
   if (e == cudaSuccess) e = tc_set_smem_limits();
   if (e == cudaSuccess) e = swap_set_smem_limits();
   if (e != cudaSuccess) {
@@ -340,12 +300,7 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   }
   c->tc_min_rows = 32;
   if (const char* v = getenv("MOE_TC_MIN_ROWS")) c->tc_min_rows = atoi(v);
-  if (const char* v = getenv("MOE_DECODE_LEGACY")) c->legacy_decode = atoi(v);
   c->last_inter_stride = scale_row_stride(I);
-  for (int f = 0; f < 3; ++f) {
-    c->s1_bps[f] = decode_s1_blocks_per_sm(f, H);
-    c->s2_bps[f] = decode_s2_blocks_per_sm(f, I);
-  }
   *out = c;
   return MOE_OK;
 }
@@ -413,9 +368,8 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   // kernels (128 weight rows x up to 64 routed rows per MMA).
   const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active &&
                       c->H <= TC_MAX_K && c->I <= TC_MAX_K;
-  const bool use_legacy = !use_tc && c->legacy_decode;
-  const bool use_sw = !use_tc && !use_legacy;
-  const int tile_m = use_tc ? TC_TILE_M : (use_sw ? 1 : kDecodeTile);
+  const bool use_sw = !use_tc;
+  const int tile_m = use_tc ? TC_TILE_M : 1;
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
   const int swkind = adt == MOE_A_BF16 ? SW_A16 : (adt == MOE_A_FP8 ? SW_A8 : SW_A4);
   const int wkind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;  // weight map type: unpacked for mxf8f6f4, packed for mxf4
@@ -442,7 +396,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     cuuint64_t xdims[2] = {xrow, (cuuint64_t)c->cap_rows}, xstr[1] = {xrow};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, ibox, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activations");
     if (ms != MOE_OK) return ms;
-  } else if (use_sw) {
+  } else {
     ms = make_w13sw_map(c, w13, wkind);
     if (ms != MOE_OK) return ms;
     ms = make_w2tc_map(c, w2, wkind);
@@ -454,32 +408,25 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows * subs}, xstr[1] = {(cuuint64_t)x_row};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, box, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activation rows");
     if (ms != MOE_OK) return ms;
-  } else {
-    ms = make_w13_map(c, w13);
-    if (ms != MOE_OK) return ms;
-    ms = make_w2_map(c, w2);
-    if (ms != MOE_OK) return ms;
   }
 
   c->ev_n = 0;
   prof_mark(c, st, "sort");
   SortOut so = sort_out(c);
-  if (use_tc || use_sw) so.pair_row = c->pair_row;
+  so.pair_row = c->pair_row;
   if (use_sw) so.active_info = c->active_info;
   cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
   if (e != cudaSuccess) return cuda_fail(e, "sort launch");
   c->last_tile_m = tile_m;
-  c->last_inter_layout = use_tc ? 1 : (use_sw && adt == MOE_A_BF16 ? 2 : 0);
+  c->last_inter_layout = use_tc ? 1 : (adt == MOE_A_BF16 ? 2 : 0);
   c->last_inter_stride = use_sw ? is_sw : scale_row_stride(c->I);
   prof_mark(c, st, "act_quant");
   if (use_tc)
     e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, 0, c->acc32, nullptr,
                            nullptr, nullptr, c->num_sms, st);
-  else if (use_sw)
+  else
     e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, xs_sw, c->acc32, w,
                            c->row_tok, c->row_w, c->num_sms, st);
-  else
-    e = launch_act_quant(x, T, c->H, fmt, c->xq, c->xs, scale_row_stride(c->H), c->acc32, c->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
 
   StageParams p{};
@@ -516,7 +463,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     prof_mark(c, st, "stage2");
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
-  } else if (use_sw) {
+  } else {
     const long u1 = max_active * (c->I / 128), u2 = max_active * ((c->H + 255) / 256);
     StageParams q1 = p1;
     q1.aq = c->xq_sorted;
@@ -532,17 +479,6 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q2.row_w = c->row_w;
     prof_mark(c, st, "stage2");
     e = launch_swap_stage(swkind, 2, q2, c->tm_w2tc, tm_inter, (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
-    if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
-  } else {
-    long items1 = max_blocks * (c->I / 32);
-    long cap1 = (long)c->num_sms * c->s1_bps[fmt];
-    prof_mark(c, st, "stage1");
-    e = launch_decode_stage1(fmt, p1, c->tm_w13, (int)(items1 < cap1 ? items1 : cap1), st);
-    if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
-    long items2 = max_blocks * (c->H / 64);
-    long cap2 = (long)c->num_sms * c->s2_bps[fmt];
-    prof_mark(c, st, "stage2");
-    e = launch_decode_stage2(fmt, p2, c->tm_w2, (int)(items2 < cap2 ? items2 : cap2), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
 
