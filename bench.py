@@ -205,14 +205,14 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def stored_traffic(kernel_name, T):
+def stored_traffic(config, kernel_name, T):
     """DRAM bytes per launch from a committed ncu summary, if it is current."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        ent = d.get("%s_T%d" % (kernel_name, T))
+        ent = d.get("%s_%s_T%d" % (config, kernel_name, T))
         if not ent:
             return None
         import hashlib
@@ -327,7 +327,7 @@ def run_ours(args, world, rank, local, pg):
     peak, peak_kind = measured_peaks()
     achieved = ab[dominant] / (per_avg[dominant] * 1e-3) / 1e9
     flops = 6.0 * n_pairs * H * I
-    traffic = stored_traffic(dominant, args.tokens)
+    traffic = stored_traffic(args.config, dominant, args.tokens)
 
     # --- sweep over the decode token tiers
     sweep = {}
@@ -366,7 +366,7 @@ def run_ours(args, world, rank, local, pg):
         "scaling": "weak",
         "vs_baseline": (round(value_us / PAGE_US[CFG.a_dtype][args.tokens], 4)
                         if (I == 384 and E == 896 and args.tokens in PAGE_US[CFG.a_dtype]) else None),
-        "dtype": {"bf16": "e2m1 x bf16 (re-encoded f16), fp32 accumulate",
+        "dtype": {"bf16": "e2m1 x bf16 (bf16 carried as five 1x32-scaled e2m1 terms), fp32 accumulate",
                   "fp8": "e2m1 x e4m3 block-scaled (1x32 e8m0), fp32 accumulate",
                   "fp4": "e2m1 x e2m1 block-scaled (1x32 e8m0), fp32 accumulate"}[CFG.a_dtype],
         "data": "synthetic (seeded; weights drawn on the GPU and MXFP4-quantised by the library)",
