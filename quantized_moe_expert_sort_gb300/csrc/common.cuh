@@ -200,15 +200,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// ~2^22 polls with back-off: several seconds at most.
-#ifndef MOE_WAIT_LIMIT
-#define MOE_WAIT_LIMIT (1u << 22)
+// Bounded waits. The pipelines hand each stage through two or three barriers,
+// so a waiting thread must wake at once: it spins on try_wait (which suspends in
+// hardware for a short while) and sleeps only after a long wait. The bound is
+// wall-clock (%globaltimer): MOE_WAIT_NS, 2 s by default.
+#ifndef MOE_WAIT_NS
+#define MOE_WAIT_NS 2000000000ull
 #endif
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t i = 0; i < MOE_WAIT_LIMIT; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
+    if ((i & 255u) == 0) {
+      if (global_ns() - t0 > MOE_WAIT_NS) break;
+      if (i > (1u << 16)) __nanosleep(128);
+    }
   }
   set_error(err, DEV_ERR_TIMEOUT);
   return false;
@@ -216,12 +230,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 
 // Wait that drains instead of hanging: once any thread of the CTA has timed
 // out (*abort set), every later wait returns false at once, so all warps run
-// to the end of their loops (meeting every named barrier) and the CTA exits.
+// to the end of their loops and the CTA exits.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
-  for (uint32_t i = 0; i < MOE_WAIT_LIMIT; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (i > 64) __nanosleep(i > 4096 ? 256 : 32);
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > MOE_WAIT_NS) break;
+      if (i > (1u << 16)) __nanosleep(128);
+    }
   }
   *abort = 1;
   set_error(err, DEV_ERR_TIMEOUT);
