@@ -30,6 +30,11 @@ enum : int {
   DEV_ERR_LAUNCH = 8,       // a kernel got less shared memory than its layout needs; it returned at once
 };
 
+// Programmatic dependent launch: wait for the previous kernel in the stream (a
+// no-op when launched without the attribute), and let the next one start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }
@@ -200,12 +205,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread in hardware until the phase completes or
+// hint_ns have passed: a waiting warp takes no issue slots from the warps that
+// share its scheduler, and wakes when the barrier completes.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
 // Bounded waits. The pipelines hand each stage through two or three barriers,
-// so a waiting thread must wake at once: it spins on try_wait (which suspends in
-// hardware for a short while) and sleeps only after a long wait. The bound is
+// so a waiting thread must wake at once, and warps that wait must not steal
+// issue slots from the TMA and MMA threads: each poll suspends in hardware
+// (woken by the phase completing) for at most MOE_SUSPEND_NS. The bound is
 // wall-clock (%globaltimer): MOE_WAIT_NS, 2 s by default.
 #ifndef MOE_WAIT_NS
 #define MOE_WAIT_NS 2000000000ull
+#endif
+#ifndef MOE_SUSPEND_NS
+#define MOE_SUSPEND_NS 1000000u
 #endif
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -217,12 +236,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (global_ns() - t0 > MOE_WAIT_NS) break;
-      if (i > (1u << 16)) __nanosleep(128);
-    }
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, MOE_SUSPEND_NS)) return true;
+    if (global_ns() - t0 > MOE_WAIT_NS) break;
   }
   set_error(err, DEV_ERR_TIMEOUT);
   return false;
@@ -234,13 +250,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort) return false;
-      if (global_ns() - t0 > MOE_WAIT_NS) break;
-      if (i > (1u << 16)) __nanosleep(128);
-    }
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, MOE_SUSPEND_NS)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > MOE_WAIT_NS) break;
   }
   *abort = 1;
   set_error(err, DEV_ERR_TIMEOUT);

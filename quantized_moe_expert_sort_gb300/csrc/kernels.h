@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda.h>
 
@@ -24,6 +25,26 @@ struct SortOut {
 constexpr int SORT_SMALL_MAX_PAIRS = 8192;  // single-CTA sort up to this many pairs
 constexpr int SORT_CHUNK = 4096;            // pairs per CTA in the multi-CTA sort
 constexpr int SORT_MAX_EXPERTS = 4096;      // shared-memory bound of the sort kernels
+
+// Kernel launch; pdl = programmatic dependent launch: the kernel may start while
+// the previous kernel in the stream drains, and waits for it (griddepcontrol.wait)
+// before it reads that kernel's results. Every kernel launched with pdl calls
+// pdl_wait() before its first dependent read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 size_t sort_small_smem(int E);
 // Text returned by moe_last_error_message() on this thread.

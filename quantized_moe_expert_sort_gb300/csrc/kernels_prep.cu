@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(1024) sort_hist_kernel(const int32_t* __restri
 // first row of chunk g's pairs of expert e.
 __global__ void __launch_bounds__(1024) sort_scan_kernel(int* __restrict__ hist, int G, int E, int tile_m, int sentinel,
                                                          SortOut so) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t smem[];
   int* cnt = reinterpret_cast<int*>(smem);
   int* cursor = cnt + E;
@@ -214,6 +216,8 @@ __global__ void __launch_bounds__(1024) sort_scan_kernel(int* __restrict__ hist,
 __global__ void __launch_bounds__(1024) sort_place_kernel(const int32_t* __restrict__ ids, long n, int E, int chunk,
                                                           const int* __restrict__ hist, int32_t* sorted_ids,
                                                           int32_t* pair_row) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(16) uint8_t smem[];
   int* cursor = reinterpret_cast<int*>(smem);
   uint8_t* wtab = reinterpret_cast<uint8_t*>(cursor + E);
@@ -342,6 +346,8 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
                                                           int sstride, float* __restrict__ acc32,
                                                           const float* __restrict__ topk_w, int32_t* __restrict__ row_tok,
                                                           float* __restrict__ row_w) {
+  pdl_wait();  // the sort's pair rows
+  pdl_launch_dependents();
   const int nb = H / 32;
   const long total = (long)T * nb;
   const long row_bytes = MODE == SW_A8 ? (long)H : H / 2;  // one (sub-)row
@@ -446,6 +452,7 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const float* __restri
 
 // out = bf16_RNE(acc32), 4 elements per thread.
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc32, long n4, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();  // the combine buffer is complete
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x) {
     float4 v = reinterpret_cast<const float4*>(acc32)[i];
     __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
@@ -472,10 +479,13 @@ cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const Sor
   int G = (int)((n + chunk - 1) / chunk);
   if (G > hist_cap_chunks) return cudaErrorInvalidValue;
   sort_hist_kernel<<<G, 1024, (size_t)E * 4, st>>>(ids, n, E, chunk, hist, err);
-  sort_scan_kernel<<<1, 1024, (size_t)E * 8 + 32 * 4, st>>>(hist, G, E, tile_m, (int)n, so);
-  sort_place_kernel<<<G, 1024, (size_t)E * 4 + (size_t)E * 32, st>>>(ids, n, E, chunk, hist, so.sorted_ids,
-                                                                     so.pair_row);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = launch_k(sort_scan_kernel, dim3(1), dim3(1024), (size_t)E * 8 + 32 * 4, st, true, hist, G, E, tile_m, (int)n, so);
+  if (e == cudaSuccess)
+    e = launch_k(sort_place_kernel, dim3(G), dim3(1024), (size_t)E * 4 + (size_t)E * 32, st, true, ids, n, E, chunk,
+                 (const int*)hist, so.sorted_ids, so.pair_row);
+  return e;
 }
 
 cudaError_t prep_set_smem_limits() {
@@ -521,15 +531,16 @@ cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, con
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const bool chunk = scale_stride == 0;
 #define MOE_SCATTER(M, C) \
-  act_scatter_kernel<M, C><<<(int)blocks, 128, 0, st>>>(xb, T, H, K, pair_row, codes, scales, scale_stride, acc32, \
-                                                        topk_w, row_tok, row_w)
-  if (mode == SW_A16) MOE_SCATTER(SW_A16, false);
-  else if (mode == SW_A8 && chunk) MOE_SCATTER(SW_A8, true);
-  else if (mode == SW_A8) MOE_SCATTER(SW_A8, false);
-  else if (chunk) MOE_SCATTER(SW_A4, true);
-  else MOE_SCATTER(SW_A4, false);
+  launch_k(act_scatter_kernel<M, C>, dim3((unsigned)blocks), dim3(128), 0, st, true, xb, T, H, K, pair_row, codes, \
+           scales, scale_stride, acc32, topk_w, row_tok, row_w)
+  cudaError_t e;
+  if (mode == SW_A16) e = MOE_SCATTER(SW_A16, false);
+  else if (mode == SW_A8 && chunk) e = MOE_SCATTER(SW_A8, true);
+  else if (mode == SW_A8) e = MOE_SCATTER(SW_A8, false);
+  else if (chunk) e = MOE_SCATTER(SW_A4, true);
+  else e = MOE_SCATTER(SW_A4, false);
 #undef MOE_SCATTER
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, uint8_t* scales, int num_sms,
@@ -548,8 +559,8 @@ cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, 
   long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  finalize_kernel<<<(int)blocks, 256, 0, st>>>(acc32, n4, reinterpret_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_k(finalize_kernel, dim3((unsigned)blocks), dim3(256), 0, st, true, acc32, n4,
+                  reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace moe

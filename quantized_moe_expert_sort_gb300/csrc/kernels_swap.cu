@@ -50,57 +50,86 @@
 namespace moe {
 namespace {
 
-constexpr int kThreadsSw = 256;
-constexpr int kEpiWarpsSw = 4;
-constexpr int kTile = 128 * 128;  // one 128-row x 128-byte operand tile
-constexpr int kURing = 32;        // items in flight in the shared-memory ring
-constexpr int kSfRing = 8;        // scale-chunk slots (a ring of its own, deeper than the operand ring)
-constexpr int kSfLag = 4;         // stages warp 1's copies run ahead of its arrivals
+constexpr int kThreadsSw = 384;
+constexpr int kEpiWarpsSw = 4;  // warps per epilogue warpgroup; two warpgroups take alternate items
 
 template <int KIND> struct SwKind;
-// kNMax: routed rows per item; kTerms: code terms per value (B rows = kTerms x rows).
+// kNMax: routed rows per item; kTerms: code terms per value (B rows = kTerms x rows);
+// kURing: items in flight in the shared-memory ring (each slot also holds the token
+// and top-k weight of its rows). SW_A8's five unpacked operand stages leave room
+// for a shorter item ring.
 template <> struct SwKind<SW_A16> {
-  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kNMax = 16, kTerms = A16_TERMS;
+  static constexpr int kNMax = 16, kTerms = A16_TERMS, kURing = 32;
   static constexpr bool kMxf4 = true;
 };
 template <> struct SwKind<SW_A8> {
-  static constexpr int kKTile = 128, kBlocks = 4, kChunks = 1, kNMax = 64, kTerms = 1;
+  static constexpr int kNMax = 64, kTerms = 1, kURing = 16;
   static constexpr bool kMxf4 = false;
 };
 template <> struct SwKind<SW_A4> {
-  static constexpr int kKTile = 256, kBlocks = 8, kChunks = 2, kNMax = 64, kTerms = 1;
+  static constexpr int kNMax = 64, kTerms = 1, kURing = 32;
   static constexpr bool kMxf4 = true;
+};
+
+// Operand pipeline of one (kind, stage).
+//   kKTile: K per stage; kRow: shared-memory bytes per operand row (the TMA box
+//   width and the swizzle span); kNS: operand stages; kSfRing: scale-chunk slots
+//   (a ring of its own, deeper than the operand ring); kSfLag: stages the scale
+//   warp's copies run ahead of its arrivals.
+// Packed e2m1 (mxf4) at stage 1 streams K = hidden in 128-byte rows (K tile 256).
+// At stage 2, K = inter is a few hundred (384 for the TP8 shard: 192 bytes per
+// row), so 128-byte boxes would leave half of every second box outside the
+// matrix; 64-byte rows (K tile 128, 64-byte swizzle) fit it exactly, and the
+// halved stages let twice as many be in flight, which this latency-bound short-K
+// stream needs. kind::mxf8f6f4 takes the weights expanded to one 16-element group
+// per 16 bytes (128-byte rows for a K tile of 128), so its tiles take twice the
+// shared memory per HBM byte.
+template <int KIND, int STAGE> struct SwCfg {
+  static constexpr bool kNarrow = SwKind<KIND>::kMxf4 && STAGE == 2;
+  static constexpr int kKTile = SwKind<KIND>::kMxf4 && !kNarrow ? 256 : 128;
+  static constexpr int kChunks = kKTile / 128;                      // 4-block scale chunks per stage
+  static constexpr int kBlocks = kKTile / 32;                       // 32-blocks per stage
+  static constexpr int kRow = SwKind<KIND>::kMxf4 ? kKTile / 2 : 128;
+  static constexpr int kXStep = SwKind<KIND>::kMxf4 ? kKTile / 2 : kKTile;  // TMA x per stage (bytes / 4-bit elements)
+  static constexpr int kKSteps = kRow / 32;                         // MMAs per tile and stage (32 bytes of K each)
+  static constexpr int kNS = kNarrow ? 9 : (SwKind<KIND>::kMxf4 ? 4 : 5);
+  static constexpr int kSfRing = kNarrow ? 16 : 8;
+  static constexpr int kSfLag = kNarrow ? 8 : 4;
+  static constexpr uint32_t kSwz = kRow == 128 ? tc::SW_128B : tc::SW_64B;
+  static constexpr int kSfCols = kChunks == 2 ? 32 : 16;            // TMEM columns per scale slot
 };
 
 template <int KIND> constexpr int acc_cols() {  // TMEM columns of one accumulator (largest MMA N)
   return (SwKind<KIND>::kTerms * SwKind<KIND>::kNMax + 15) / 16 * 16;
 }
 
-// Operand pipeline depth: the unpacked (16U4) weight tiles of kind::mxf8f6f4 take
-// twice the shared memory per HBM byte, so that kind gets one more stage.
-template <int KIND> constexpr int sw_stages() { return SwKind<KIND>::kMxf4 ? 4 : 5; }
-
 struct UItem {
   int e, tile, row0, nrows;  // nrows < 0: end of work
 };
 
-template <int KIND> struct SwLayout {
-  static constexpr int kNS = sw_stages<KIND>();
-  static constexpr uint32_t a_bytes = 2 * kTile;                      // two 128-row weight tiles
-  static constexpr uint32_t b_bytes = acc_cols<KIND>() * 128;          // B rows = terms x routed rows
-  static constexpr uint32_t sf_bytes = 3 * 1024;                       // sfa gate, sfa up, sfb
+template <int KIND, int STAGE> struct SwLayout {
+  using C = SwCfg<KIND, STAGE>;
+  static constexpr int kNS = C::kNS;
+  static constexpr int kURing = SwKind<KIND>::kURing, kSfRing = C::kSfRing;
+  static constexpr uint32_t tile_bytes = 128 * C::kRow;                // one 128-row operand tile
+  static constexpr uint32_t a_bytes = 2 * tile_bytes;                  // two weight tiles
+  static constexpr uint32_t b_bytes = acc_cols<KIND>() * C::kRow;      // B rows = terms x routed rows
+  static constexpr uint32_t sf_op = C::kChunks * 512;                  // one operand's chunks
+  static constexpr uint32_t sf_bytes = 3 * sf_op;                      // sfa tile 0, sfa tile 1, sfb
   static constexpr uint32_t a = 0;
   static constexpr uint32_t b = a + kNS * a_bytes;
   static constexpr uint32_t sf = b + kNS * b_bytes;
   static constexpr uint32_t items = sf + kSfRing * sf_bytes;
-  static constexpr uint32_t bars = items + kURing * sizeof(UItem);
-  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 2 * kURing + kSfRing + 1) * 8;
+  static constexpr uint32_t rows = items + kURing * sizeof(UItem);     // per slot: int tok[kNMax], float w[kNMax]
+  static constexpr uint32_t row_bytes = 8 * SwKind<KIND>::kNMax;
+  static constexpr uint32_t bars = rows + kURing * row_bytes;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 3 * kURing + kSfRing + 1) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;  // + alignment slack
 };
 
 constexpr uint32_t kTmemColsSw = 512;
-// TMEM: accumulators (2 buffers x 2 tiles) from column 0, then the scale slots,
-// 32 columns per operand slot.
+// TMEM: accumulators (2 buffers x 2 tiles) from column 0, then one scale slot per
+// operand stage: [sfa tile 0 | sfa tile 1 | sfb], 4 columns per 4-block chunk.
 template <int KIND> constexpr uint32_t sf_col0() { return 4 * acc_cols<KIND>(); }
 
 __device__ __forceinline__ void tma_load_2d_sw(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
@@ -115,6 +144,11 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// One arrival on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
@@ -139,7 +173,9 @@ __device__ __forceinline__ uint32_t sf_off_sw(int m) { return 16u * (m & 31) + 4
 
 // Weight tile bytes one TMA load reports: packed global bytes (see the
 // 16U4_ALIGN16B note of the prefill kernels), 16 KB for packed e2m1.
-template <int KIND> constexpr uint32_t w_tile_tx() { return SwKind<KIND>::kMxf4 ? kTile : kTile / 2; }
+template <int KIND, int STAGE> constexpr uint32_t w_tile_tx() {
+  return SwKind<KIND>::kMxf4 ? SwLayout<KIND, STAGE>::tile_bytes : SwLayout<KIND, STAGE>::tile_bytes / 2;
+}
 
 }  // namespace
 
@@ -147,11 +183,15 @@ template <int KIND, int STAGE>
 __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p, const __grid_constant__ CUtensorMap tm_w,
                                                                    const __grid_constant__ CUtensorMap tm_x) {
   using KD = SwKind<KIND>;
-  using L = SwLayout<KIND>;
+  using L = SwLayout<KIND, STAGE>;
+  using C = SwCfg<KIND, STAGE>;
   constexpr int kNS = L::kNS;
   constexpr int NMAX = KD::kNMax;
   constexpr int kAccCols = acc_cols<KIND>();
-  static_assert(4 * kAccCols + sw_stages<KIND>() * 32 <= 512, "TMEM columns");
+  constexpr int kURing = KD::kURing, kSfRing = C::kSfRing, kSfLag = C::kSfLag;
+  constexpr int kEpiGroups = STAGE == 2 ? 2 : 1;  // epilogue warpgroups (one per accumulator buffer at stage 2)
+  static_assert(4 * kAccCols + kNS * C::kSfCols <= (int)kTmemColsSw, "TMEM columns");
+  static_assert(kSfRing > kSfLag && L::total <= 232448, "shared memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
@@ -160,7 +200,8 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
   uint64_t* tempty = tfull + 2;
   uint64_t* ufull = tempty + 2;
   uint64_t* uempty = ufull + kURing;
-  uint64_t* sfempty = uempty + kURing;  // scale-ring slot free (MMA commit)
+  uint64_t* rfull = uempty + kURing;    // the slot's row tokens / weights have landed (stage 2)
+  uint64_t* sfempty = rfull + kURing;   // scale-ring slot free (MMA commit)
   uint64_t* drain = sfempty + kSfRing;
   UItem* items = reinterpret_cast<UItem*>(smem + L::items);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
@@ -173,7 +214,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, I = p.I;
   const int kdim = STAGE == 1 ? H : I;
-  const int ktiles = (kdim + KD::kKTile - 1) / KD::kKTile;
+  const int ktiles = (kdim + C::kKTile - 1) / C::kKTile;
   const int nblk_k = kdim / 32;
   const int ntn = STAGE == 1 ? I / 128 : (H + 255) / 256;  // units per expert
 
@@ -182,7 +223,11 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
     for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kEpiWarpsSw); }
     // an item is released by the TMA issuer, the scale warp, the MMA issuer and the epilogue warps
-    for (int s = 0; s < kURing; ++s) { mbar_init(&ufull[s], 1); mbar_init(&uempty[s], 3 + kEpiWarpsSw); }
+    for (int s = 0; s < kURing; ++s) {
+      mbar_init(&ufull[s], 1);
+      mbar_init(&uempty[s], 3 + kEpiWarpsSw);
+      mbar_init(&rfull[s], 32);  // one cp.async-tracking arrival per scheduler lane
+    }
     for (int s = 0; s < kSfRing; ++s) mbar_init(&sfempty[s], 1);
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -201,6 +246,9 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
+  // everything above overlapped the previous kernel's tail; its results are read from here on
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 3) {
     // ------------------------------ item scheduler ------------------------------
@@ -237,7 +285,30 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
             mbar_arrive(&ufull[us]);
           }
           __syncwarp();
-          if (!more) { done = true; break; }
+          if (!more) {
+            // a second end marker: at stage 2 the two epilogue warpgroups take
+            // alternate items and each must meet one
+            const int ue = (it + 1) % kURing;
+            if (warp_wait(&uempty[ue], (((it + 1) / kURing) & 1) ^ 1, p.err, &abort_flag) && lane == 0) {
+              items[ue].nrows = -1;
+              mbar_arrive(&ufull[ue]);
+            }
+            __syncwarp();
+            done = true;
+            break;
+          }
+          if (STAGE == 2) {
+            // token and top-k weight of the item's rows, copied into the slot while
+            // the item waits in the ring (only the epilogue reads them)
+            const int r0 = ol + ch * NMAX, nr = min(NMAX, cl - ch * NMAX);
+            int* rt = reinterpret_cast<int*>(smem + L::rows + us * L::row_bytes);
+            float* rw = reinterpret_cast<float*>(rt + NMAX);
+            for (int n = lane; n < nr; n += 32) {
+              cp_async4(rt + n, p.row_tok + r0 + n);
+              cp_async4(rw + n, p.row_w + r0 + n);
+            }
+            cp_async_arrive_noinc(&rfull[us]);
+          }
         }
       }
     }
@@ -277,24 +348,25 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         prefetch_scales(it);
         const int nsub = ui.nrows * KD::kTerms;  // B rows: the item's sub-rows
         const int nbox = (nsub + 15) / 16;
-        const uint32_t btx = (uint32_t)nbox * 16 * 128;
+        const uint32_t btx = (uint32_t)nbox * 16 * C::kRow;
         for (int ks = 0; ks < ktiles; ++ks, ++stage) {
           const int slot = stage % kNS;
           if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + L::a + slot * L::a_bytes;
           uint8_t* sb = smem + L::b + slot * L::b_bytes;
-          mbar_arrive_expect_tx(&full[slot], 2 * w_tile_tx<KIND>() + btx);
+          mbar_arrive_expect_tx(&full[slot], 2 * w_tile_tx<KIND, STAGE>() + btx);
+          const int kx = ks * C::kXStep;
           if (STAGE == 1) {
-            tma_load_4d(sa, &tm_w, ks * 128, ui.tile * 128, 0, ui.e, &full[slot]);
-            tma_load_4d(sa + kTile, &tm_w, ks * 128, ui.tile * 128, 1, ui.e, &full[slot]);
+            tma_load_4d(sa, &tm_w, kx, ui.tile * 128, 0, ui.e, &full[slot]);
+            tma_load_4d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 128, 1, ui.e, &full[slot]);
           } else {  // rows past H (odd H / 128) are filled with zeros
-            tma_load_3d(sa, &tm_w, ks * 128, ui.tile * 256, ui.e, &full[slot]);
-            tma_load_3d(sa + kTile, &tm_w, ks * 128, ui.tile * 256 + 128, ui.e, &full[slot]);
+            tma_load_3d(sa, &tm_w, kx, ui.tile * 256, ui.e, &full[slot]);
+            tma_load_3d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 256 + 128, ui.e, &full[slot]);
           }
           // routed rows: contiguous sub-rows [row0 * kTerms, (row0 + nrows) * kTerms), 16-row boxes
           // (rows past this expert belong to later experts and only fill unused columns)
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d_sw(sb + bx * 16 * 128, &tm_x, ks * 128, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
+            tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, kx, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
         }
       }
     }
@@ -333,23 +405,23 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
       for (int ks = 0; ks < ktiles && ok; ++ks) {
         const int fslot = stage % kSfRing;
         if (!warp_wait(&sfempty[fslot], ((stage / kSfRing) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
-        uint8_t* sf = smem + L::sf + fslot * L::sf_bytes;  // [sfa tile 0 | sfa tile 1 | sfb], 1 KB each
-        for (int c = 0; c < KD::kChunks; ++c) {
-          const int kb0 = ks * KD::kBlocks + 4 * c;
+        uint8_t* sf = smem + L::sf + fslot * L::sf_bytes;  // [sfa tile 0 | sfa tile 1 | sfb], sf_op bytes each
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int kb0 = ks * C::kBlocks + 4 * c;
           if (kb0 < nblk_k) {  // kdim % 128 == 0: a chunk is all in or all out
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int m = 4 * lane + i;
               cp_async4(sf + 512 * c + sf_off_sw(m), wsrc + (size_t)m * sb_w + kb0);
-              if (t1) cp_async4(sf + 1024 + 512 * c + sf_off_sw(m), wsrc + (w1 + m) * sb_w + kb0);
+              if (t1) cp_async4(sf + L::sf_op + 512 * c + sf_off_sw(m), wsrc + (w1 + m) * sb_w + kb0);
             }
             for (int n = lane; n < nsub; n += 32)
-              cp_async4(sf + 2048 + 512 * c + sf_off_sw(n), p.as + (sub0 + n) * p.xs_stride + kb0);
+              cp_async4(sf + 2 * L::sf_op + 512 * c + sf_off_sw(n), p.as + (sub0 + n) * p.xs_stride + kb0);
           } else {  // past the end of K: neutral scales (the operands there are zero)
             const uint4 n127 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
             *reinterpret_cast<uint4*>(sf + 512 * c + 16 * lane) = n127;
-            *reinterpret_cast<uint4*>(sf + 1024 + 512 * c + 16 * lane) = n127;
-            *reinterpret_cast<uint4*>(sf + 2048 + 512 * c + 16 * lane) = n127;
+            *reinterpret_cast<uint4*>(sf + L::sf_op + 512 * c + 16 * lane) = n127;
+            *reinterpret_cast<uint4*>(sf + 2 * L::sf_op + 512 * c + 16 * lane) = n127;
           }
         }
         cp_async_commit();
@@ -372,8 +444,10 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
     // 16-byte-unit offsets to their start-address field, and the ring positions
     // are counters rather than divisions.
     if (lane == 0) {
-      const uint64_t dA0 = tc::sdesc(smem_u32(smem + L::a), 16, 1024, tc::SW_128B);
-      const uint64_t dB0 = tc::sdesc(smem_u32(smem + L::b), 16, 1024, tc::SW_128B);
+      // K-major, swizzled: 8-row groups kRow * 8 bytes apart; a K step advances the
+      // start address by 32 bytes inside the swizzle span
+      const uint64_t dA0 = tc::sdesc(smem_u32(smem + L::a), 16, 8 * C::kRow, C::kSwz);
+      const uint64_t dB0 = tc::sdesc(smem_u32(smem + L::b), 16, 8 * C::kRow, C::kSwz);
       const uint64_t dS0 = tc::sdesc(smem_u32(smem + L::sf), 0, 128, tc::SW_NONE);
       const uint32_t sf0 = tbase + sf_col0<KIND>();
       int slot = 0, fslot = 0;
@@ -397,29 +471,34 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         for (int ks = 0; ks < ktiles; ++ks) {
           if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag)) { ok = false; break; }
           tc::fence_after();
-          const uint32_t sfc = sf0 + slot * 32;  // sfa tile 0 +0, sfa tile 1 +8, sfb +16
+          constexpr uint32_t kOpCols = 4 * C::kChunks;  // TMEM columns of one operand's scale chunks
+          const uint32_t sfc = sf0 + slot * C::kSfCols;  // sfa tile 0, sfa tile 1, sfb: kOpCols apart
           const uint64_t ds = dS0 + (uint64_t)((fslot * L::sf_bytes) >> 4);
+          const int kleft = kdim - ks * C::kKTile;  // K of this tile inside the matrix (> 0)
 #pragma unroll
-          for (int c = 0; c < KD::kChunks; ++c) {
+          for (int c = 0; c < C::kChunks; ++c) {
+            if (c > 0 && 128 * c >= kleft) break;  // a chunk wholly past the end of K is not used
             tc::cp_32x128b_warpx4(sfc + 4 * c, ds + (512 * c >> 4));
-            tc::cp_32x128b_warpx4(sfc + 8 + 4 * c, ds + ((1024 + 512 * c) >> 4));
-            tc::cp_32x128b_warpx4(sfc + 16 + 4 * c, ds + ((2048 + 512 * c) >> 4));
+            tc::cp_32x128b_warpx4(sfc + kOpCols + 4 * c, ds + ((L::sf_op + 512 * c) >> 4));
+            tc::cp_32x128b_warpx4(sfc + 2 * kOpCols + 4 * c, ds + ((2 * L::sf_op + 512 * c) >> 4));
           }
           const uint64_t da = dA0 + (uint64_t)((slot * L::a_bytes) >> 4);
           const uint64_t db = dB0 + (uint64_t)((slot * L::b_bytes) >> 4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < C::kKSteps; ++i) {
+            if (i > 0 && i * (C::kKTile / C::kKSteps) >= kleft) break;  // K steps past the end of K
             const uint32_t acc = (ks > 0 || i > 0) ? 1u : 0u;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-              const uint64_t dai = da + ((g * kTile + 32 * i) >> 4);
+              const uint64_t dai = da + ((g * L::tile_bytes + 32 * i) >> 4);
               const uint64_t dbi = db + ((32 * i) >> 4);
               if (KD::kMxf4) {  // scale_vec::2X: K block pair 2(i&1), 2(i&1)+1 of chunk i/2
                 const uint32_t id = id0 | ((2u * (i & 1)) << 4) | ((2u * (i & 1)) << 29);
-                tc::mma_mxf4(dg + g * kAccCols, dai, dbi, id, sfc + 8 * g + 4 * (i >> 1), sfc + 16 + 4 * (i >> 1), acc);
+                tc::mma_mxf4(dg + g * kAccCols, dai, dbi, id, sfc + kOpCols * g + 4 * (i >> 1),
+                             sfc + 2 * kOpCols + 4 * (i >> 1), acc);
               } else {
                 const uint32_t id = id0 | ((uint32_t)i << 4) | ((uint32_t)i << 29);
-                tc::mma_mxf8f6f4(dg + g * kAccCols, dai, dbi, id, sfc + 8 * g, sfc + 16, acc);
+                tc::mma_mxf8f6f4(dg + g * kAccCols, dai, dbi, id, sfc + kOpCols * g, sfc + 2 * kOpCols, acc);
               }
             }
           }
@@ -435,13 +514,18 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
       tc::commit(drain);
       mbar_wait(drain, 0, p.err);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && (warp - 4) / kEpiWarpsSw < kEpiGroups) {
     // ------------------------------ epilogue ------------------------------
-    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    // Stage 2: warpgroup wg (warps 4-7, 8-11) takes items wg, wg + 2, ... and so
+    // accumulator buffer wg, so one warpgroup's TMEM loads overlap the other's
+    // global reductions (its items are short). Stage 1 (long items) runs one
+    // warpgroup over both buffers; warps 8-11 stay idle there.
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int wg = (warp - 4) / kEpiWarpsSw;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-    int tok_a = 0, tok_b = 0, nt_a = 0, nt_b = 0;
-    float w_a = 0.0f, w_b = 0.0f, nw_a = 0.0f, nw_b = 0.0f;
-    int it = 0;
+    int tok_a = 0, tok_b = 0;
+    float w_a = 0.0f, w_b = 0.0f;
+    int it = wg;
     while (true) {
       const int us = it % kURing;
       if (!warp_wait(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
@@ -449,52 +533,48 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
       if (ui.nrows < 0) break;
       const int nrows = ui.nrows, row0 = ui.row0;
       __syncwarp();
-      if (lane == 0) mbar_arrive_relaxed(&uempty[us]);  // the item is in registers
-      // stage 2: token and top-k weight of the item's rows (lanes n and 32 + n); those of
-      // the next item are fetched now, so their latency hides behind this item's work
       if (STAGE == 2) {
-        if (it == 0) {
-          tok_a = lane < nrows ? p.row_tok[row0 + lane] : 0;
-          w_a = lane < nrows ? p.row_w[row0 + lane] : 0.0f;
-          tok_b = 32 + lane < nrows ? p.row_tok[row0 + 32 + lane] : 0;
-          w_b = 32 + lane < nrows ? p.row_w[row0 + 32 + lane] : 0.0f;
-        } else {
-          tok_a = nt_a; w_a = nw_a; tok_b = nt_b; w_b = nw_b;
+        // token and top-k weight of the item's rows (lanes n and 32 + n), staged in
+        // the slot by the scheduler long before the item reaches the epilogue
+        if (!warp_wait(&rfull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
+        const int* rt = reinterpret_cast<const int*>(smem + L::rows + us * L::row_bytes);
+        const float* rw = reinterpret_cast<const float*>(rt + NMAX);
+        tok_a = lane < nrows ? rt[lane] : 0;
+        w_a = lane < nrows ? rw[lane] : 0.0f;
+        if (NMAX > 32) {
+          tok_b = 32 + lane < nrows ? rt[32 + lane] : 0;
+          w_b = 32 + lane < nrows ? rw[32 + lane] : 0.0f;
         }
-        const int un = (it + 1) % kURing;
-        if (!warp_wait(&ufull[un], ((it + 1) / kURing) & 1, p.err, &abort_flag)) break;
-        const UItem nx = items[un];
-        if (nx.nrows > 0) {
-          nt_a = lane < nx.nrows ? p.row_tok[nx.row0 + lane] : 0;
-          nw_a = lane < nx.nrows ? p.row_w[nx.row0 + lane] : 0.0f;
-          nt_b = 32 + lane < nx.nrows ? p.row_tok[nx.row0 + 32 + lane] : 0;
-          nw_b = 32 + lane < nx.nrows ? p.row_w[nx.row0 + 32 + lane] : 0.0f;
-        }
+        // (the slot is released after the stores below, which consume these values)
+      } else if (lane == 0) {
+        mbar_arrive_relaxed(&uempty[us]);  // the item is in registers
       }
       const int buf = it & 1;
       if (!warp_wait(&tfull[buf], (it >> 1) & 1, p.err, &abort_flag)) break;
-      ++it;  // (warp_wait reconverged the warp: tcgen05.ld is .sync.aligned)
+      it += kEpiGroups;  // (warp_wait reconverged the warp: tcgen05.ld is .sync.aligned)
       tc::fence_after();
       const uint32_t dg = tbase + lane_off + buf * 2 * kAccCols;
-      // Values of item rows [c0, c0 + 16) of one accumulator: row n sums columns
-      // n * kTerms + t (its code terms); only the chunks of 16 columns in use are read.
-      auto load_cols = [&](uint32_t acc, int c0, float* v) {
-        constexpr int kCh = KD::kTerms;  // 16 rows x kTerms columns = kTerms chunks of 16
-        uint32_t r[kCh][16];
-        const int nch = (min(16, nrows - c0) * KD::kTerms + 15) / 16;
+      // Values of item rows [c0, c0 + 16) of both accumulators: row n sums columns
+      // n * kTerms + t (its code terms, in order of t); only the chunks of 16
+      // columns in use are read, both accumulators' chunk under one wait.
+      auto load_pair = [&](uint32_t acc0, uint32_t acc1, int c0, float* v0, float* v1) {
+        const int nch = (min(16, nrows - c0) * KD::kTerms + 15) / 16;  // warp-uniform
 #pragma unroll
-        for (int ch = 0; ch < kCh; ++ch)
-          if (ch < nch) tc::ld_32x32b_x16(acc + c0 * KD::kTerms + 16 * ch, r[ch]);
-        tc::ld_wait();
+        for (int n = 0; n < 16; ++n) { v0[n] = 0.0f; v1[n] = 0.0f; }
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          float a = 0.0f;
+        for (int ch = 0; ch < KD::kTerms; ++ch) {  // 16 rows x kTerms columns = kTerms chunks of 16
+          if (ch < nch) {
+            uint32_t r0[16], r1[16];
+            tc::ld_32x32b_x16(acc0 + c0 * KD::kTerms + 16 * ch, r0);
+            tc::ld_32x32b_x16(acc1 + c0 * KD::kTerms + 16 * ch, r1);
+            tc::ld_wait();
 #pragma unroll
-          for (int t = 0; t < KD::kTerms; ++t) {
-            const int col = n * KD::kTerms + t;
-            if (col / 16 < nch) a += __uint_as_float(r[col / 16][col % 16]);
+            for (int j = 0; j < 16; ++j) {
+              const int n = (16 * ch + j) / KD::kTerms;
+              v0[n] += __uint_as_float(r0[j]);
+              v1[n] += __uint_as_float(r1[j]);
+            }
           }
-          v[n] = a;
         }
       };
       // after the item's last TMEM load the accumulator goes back to the MMA warp,
@@ -510,8 +590,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         const int j = ui.tile * 128 + 32 * q + lane;  // intermediate column of this lane
         for (int c0 = 0; c0 < nrows; c0 += 16) {
           float gv[16], uv[16];
-          load_cols(dg, c0, gv);
-          load_cols(dg + kAccCols, c0, uv);
+          load_pair(dg, dg + kAccCols, c0, gv, uv);
           release_acc(c0);
           const int nn = min(16, nrows - c0);
 #pragma unroll
@@ -552,8 +631,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         const bool h1ok = h0 + 128 < H;
         for (int c0 = 0; c0 < nrows; c0 += 16) {
           float v0[16], v1[16];
-          load_cols(dg, c0, v0);
-          load_cols(dg + kAccCols, c0, v1);
+          load_pair(dg, dg + kAccCols, c0, v0, v1);
           release_acc(c0);
           const int nn = min(16, nrows - c0);
 #pragma unroll
@@ -568,6 +646,8 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&uempty[us]);  // the row values have been consumed
       }
     }
   }
@@ -584,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
 template <int KIND, int STAGE>
 static cudaError_t set_limit_sw() {
   return cudaFuncSetAttribute(swap_stage_kernel<KIND, STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)SwLayout<KIND>::total);
+                              (int)SwLayout<KIND, STAGE>::total);
 }
 
 cudaError_t swap_set_smem_limits() {
@@ -598,20 +678,20 @@ cudaError_t swap_set_smem_limits() {
 }
 
 template <int KIND>
-static void launch_sw(int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x, int grid,
-                      cudaStream_t st) {
+static cudaError_t launch_sw(int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                             int grid, cudaStream_t st) {
   if (stage == 1)
-    swap_stage_kernel<KIND, 1><<<grid, kThreadsSw, SwLayout<KIND>::total, st>>>(p, tm_w, tm_x);
-  else
-    swap_stage_kernel<KIND, 2><<<grid, kThreadsSw, SwLayout<KIND>::total, st>>>(p, tm_w, tm_x);
+    return launch_k(swap_stage_kernel<KIND, 1>, dim3(grid), dim3(kThreadsSw), SwLayout<KIND, 1>::total, st, true, p, tm_w,
+                    tm_x);
+  return launch_k(swap_stage_kernel<KIND, 2>, dim3(grid), dim3(kThreadsSw), SwLayout<KIND, 2>::total, st, true, p, tm_w,
+                  tm_x);
 }
 
 cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               int grid, cudaStream_t st) {
-  if (kind == SW_A16) launch_sw<SW_A16>(stage, p, tm_w, tm_x, grid, st);
-  else if (kind == SW_A8) launch_sw<SW_A8>(stage, p, tm_w, tm_x, grid, st);
-  else launch_sw<SW_A4>(stage, p, tm_w, tm_x, grid, st);
-  return cudaGetLastError();
+  if (kind == SW_A16) return launch_sw<SW_A16>(stage, p, tm_w, tm_x, grid, st);
+  if (kind == SW_A8) return launch_sw<SW_A8>(stage, p, tm_w, tm_x, grid, st);
+  return launch_sw<SW_A4>(stage, p, tm_w, tm_x, grid, st);
 }
 
 }  // namespace moe

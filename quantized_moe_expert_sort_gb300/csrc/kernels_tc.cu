@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
+  // everything above overlapped the previous kernel's tail; its results are read from here on
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -431,11 +434,11 @@ cudaError_t tc_set_smem_limits() {
 cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                             int grid, cudaStream_t st) {
   const size_t smem = TcLayout::total;
-  if (kind == TC_A8W4 && stage == 1) tc_stage_kernel<TC_A8W4, 1><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
-  else if (kind == TC_A8W4) tc_stage_kernel<TC_A8W4, 2><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
-  else if (stage == 1) tc_stage_kernel<TC_A4W4, 1><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
-  else tc_stage_kernel<TC_A4W4, 2><<<grid, kThreadsTc, smem, st>>>(p, tm_a, tm_b);
-  return cudaGetLastError();
+  const dim3 g(grid), b(kThreadsTc);
+  if (kind == TC_A8W4 && stage == 1) return launch_k(tc_stage_kernel<TC_A8W4, 1>, g, b, smem, st, true, p, tm_a, tm_b);
+  if (kind == TC_A8W4) return launch_k(tc_stage_kernel<TC_A8W4, 2>, g, b, smem, st, true, p, tm_a, tm_b);
+  if (stage == 1) return launch_k(tc_stage_kernel<TC_A4W4, 1>, g, b, smem, st, true, p, tm_a, tm_b);
+  return launch_k(tc_stage_kernel<TC_A4W4, 2>, g, b, smem, st, true, p, tm_a, tm_b);
 }
 
 }  // namespace moe

@@ -83,6 +83,7 @@ struct moe_ctx {
   const void* tm_w13tc_key; int tm_w13tc_kind; CUtensorMap tm_w13tc;
   const void* tm_w2tc_key; int tm_w2tc_kind; CUtensorMap tm_w2tc;
   const void* tm_w13sw_key; int tm_w13sw_kind; CUtensorMap tm_w13sw;  // 128-row gate / up tiles
+  const void* tm_w2sw_key; CUtensorMap tm_w2sw;  // packed w2, 64-byte rows (few-rows stage 2)
   int last_inter_stride;
   int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
   int last_inter_layout;
@@ -144,6 +145,21 @@ static moe_status make_w13tc_map(moe_ctx* c, const uint8_t* w13, int kind) {
   if (s != MOE_OK) return s;
   c->tm_w13tc_key = w13;
   c->tm_w13tc_kind = kind;
+  return MOE_OK;
+}
+
+// Packed w2 in 64-byte rows (K tile 128, 64-byte swizzle) for the few-rows mxf4
+// stage 2, whose K = inter is too short for 128-byte boxes to be filled.
+static moe_status make_w2sw_map(moe_ctx* c, const uint8_t* w2) {
+  if (c->tm_w2sw_key == w2) return MOE_OK;
+  const cuuint64_t H = c->H, I = c->I, E = c->E;
+  cuuint64_t dims[3] = {I / 2, H, E};
+  cuuint64_t strides[2] = {I / 2, H * I / 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  moe_status s = encode(&c->tm_w2sw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w2, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_64B, "w2 fp4 packed, 64-byte rows");
+  if (s != MOE_OK) return s;
+  c->tm_w2sw_key = w2;
   return MOE_OK;
 }
 
@@ -399,11 +415,14 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   } else {
     ms = make_w13sw_map(c, w13, wkind);
     if (ms != MOE_OK) return ms;
-    ms = make_w2tc_map(c, w2, wkind);
+    // stage 2 streams K = inter: 64-byte rows for packed e2m1, 128-byte (unpacked) rows for A8
+    ms = adt == MOE_A_FP8 ? make_w2tc_map(c, w2, wkind) : make_w2sw_map(c, w2);
     if (ms != MOE_OK) return ms;
     cuuint32_t box[2] = {128, 16};
+    cuuint32_t ibox[2] = {adt == MOE_A_FP8 ? 128u : 64u, 16};
     cuuint64_t idims[2] = {(cuuint64_t)i_row, (cuuint64_t)c->cap_rows * subs}, istr[1] = {(cuuint64_t)i_row};
-    ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, box, CU_TENSOR_MAP_SWIZZLE_128B, "intermediate rows");
+    ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, ibox,
+                adt == MOE_A_FP8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "intermediate rows");
     if (ms != MOE_OK) return ms;
     cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows * subs}, xstr[1] = {(cuuint64_t)x_row};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, box, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activation rows");
@@ -478,7 +497,8 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q2.row_tok = c->row_tok;
     q2.row_w = c->row_w;
     prof_mark(c, st, "stage2");
-    e = launch_swap_stage(swkind, 2, q2, c->tm_w2tc, tm_inter, (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
+    e = launch_swap_stage(swkind, 2, q2, adt == MOE_A_FP8 ? c->tm_w2tc : c->tm_w2sw, tm_inter,
+                          (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
 
