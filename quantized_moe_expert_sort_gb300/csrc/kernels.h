@@ -121,6 +121,9 @@ cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtens
 enum { SW_A16 = 0, SW_A8 = 1, SW_A4 = 2 };
 constexpr int A16_TERMS = 5;  // e2m1 code terms carrying one bf16 value (few-rows path)
 cudaError_t swap_set_smem_limits();
+// Shared-memory bytes per operand row (TMA box width) of the few-rows kernels'
+// (kind, stage): the tensor maps the host encodes must use this box width.
+int swap_row_bytes(int kind, int stage);
 cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               int grid, cudaStream_t st);
 

@@ -334,8 +334,8 @@ __device__ __forceinline__ uint32_t block_scale_of(float amax, int emax, float* 
   return (uint32_t)(E + 127);
 }
 
-// Quantise one token's 32-block per thread and write it to the sorted rows of
-// the token's K routed pairs (see launch_act_scatter). A16: A16_TERMS e2m1
+// Quantise each 32-block of a token (four threads per block) and write it to the
+// sorted rows of the token's K routed pairs (see launch_act_scatter). A16: A16_TERMS e2m1
 // terms per value, term t quantising (MX rule) what terms 0..t-1 left over (in
 // fp32 the residual v - code * 2^E is exact), term t of sorted row r written as
 // sub-row r * A16_TERMS + t.
@@ -348,59 +348,73 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
                                                           float* __restrict__ row_w) {
   pdl_wait();  // the sort's pair rows
   pdl_launch_dependents();
+  // Four threads (a quad of lanes) per (token, 32-block): thread q holds elements
+  // 8q..8q+7, the block maximum is reduced across the quad, and the quad's threads
+  // take the top-k destinations k = q, q + 4, ... (each writes the whole block).
+  constexpr int kTerms = MODE == SW_A16 ? A16_TERMS : 1;
+  constexpr int kWords = MODE == SW_A8 ? 2 : 1;  // code words per thread and term (8 e4m3 / 8 e2m1)
   const int nb = H / 32;
   const long total = (long)T * nb;
   const long row_bytes = MODE == SW_A8 ? (long)H : H / 2;  // one (sub-)row
-  const long nthreads = (long)gridDim.x * blockDim.x;
-  for (long w = (long)blockIdx.x * blockDim.x + threadIdx.x; w < total; w += nthreads) {
-    const long t = w / nb;
-    const int b = (int)(w % nb);
-    const uint4* src = reinterpret_cast<const uint4*>(x + t * H + 32 * b);
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 q = __ldg(src + i);
-      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+  const int lane = threadIdx.x & 31, q = lane & 3, qbase = lane & ~3;
+  const long warps = (long)gridDim.x * (blockDim.x / 32);
+  // warp-uniform loop: 8 blocks per warp and pass, every lane runs every pass
+  for (long w0 = ((long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * 8; w0 < total; w0 += warps * 8) {
+    const long w = w0 + (lane >> 2);
+    const bool valid = w < total;
+    const long t = valid ? w / nb : 0;
+    const int b = valid ? (int)(w % nb) : 0;
+    float v[8];
+    {
+      const uint4 qd = valid ? __ldg(reinterpret_cast<const uint4*>(x + t * H + 32 * b) + q) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t wd[4] = {qd.x, qd.y, qd.z, qd.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        v[8 * i + 2 * j] = __uint_as_float(wd[j] << 16);
-        v[8 * i + 2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
+        v[2 * j] = __uint_as_float(wd[j] << 16);
+        v[2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
       }
     }
-    constexpr int kTerms = MODE == SW_A16 ? A16_TERMS : 1;
-    uint32_t c[kTerms][8];  // codes per term: e4m3 bytes (A8) or e2m1 pairs in c[t][0..3] (A4, A16)
-    uint32_t sc[kTerms];    // e8m0 scale byte per term
+    uint32_t c[kTerms][kWords];  // this thread's codes per term
+    uint32_t sc[kTerms];         // e8m0 scale byte per term (the same in the quad)
 #pragma unroll
     for (int tt = 0; tt < kTerms; ++tt) {
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
       float mul;
       if (MODE == SW_A8) {
         sc[tt] = block_scale_of(amax, 8, &mul);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 2; ++i)
           c[tt][i] = cvt_e4m3x2(__fmul_rn(v[4 * i], mul), __fmul_rn(v[4 * i + 1], mul)) |
                      (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], mul), __fmul_rn(v[4 * i + 3], mul)) << 16);
       } else {
         sc[tt] = block_scale_of(amax, 2, &mul);
+        uint32_t acc = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t acc = 0;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            acc |= cvt_e2m1x2(__fmul_rn(v[8 * i + 2 * k], mul), __fmul_rn(v[8 * i + 2 * k + 1], mul)) << (8 * k);
-          c[tt][i] = acc;
-        }
+        for (int k = 0; k < 4; ++k)
+          acc |= cvt_e2m1x2(__fmul_rn(v[2 * k], mul), __fmul_rn(v[2 * k + 1], mul)) << (8 * k);
+        c[tt][0] = acc;
         if (tt + 1 < kTerms) {
           // A16: the next term quantises the exact residual of this one
           const float sv = e8m0_to_f32(sc[tt]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] -= e2m1_to_f32((c[tt][i >> 3] >> (4 * (i & 7))) & 0xFu) * sv;
+          for (int i = 0; i < 8; ++i) v[i] -= e2m1_to_f32((acc >> (4 * i)) & 0xFu) * sv;
         }
       }
     }
-    for (int k = 0; k < K; ++k) {
+    // the whole block's codes in every thread of the quad
+    uint32_t full[kTerms][4 * kWords];
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt)
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) full[tt][kWords * s + i] = __shfl_sync(0xFFFFFFFFu, c[tt][i], qbase + s);
+    if (!valid) continue;
+    for (int k = q; k < K; k += 4) {
       const int r = __ldg(pair_row + t * K + k);
       if (r < 0) continue;
       if (row_tok && b == 0) {
@@ -410,13 +424,13 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
       uint8_t* dst = codes + (size_t)r * kTerms * row_bytes;
       if (MODE == SW_A8) {
         uint4* d0 = reinterpret_cast<uint4*>(dst + 32 * b);
-        d0[0] = make_uint4(c[0][0], c[0][1], c[0][2], c[0][3]);
-        d0[1] = make_uint4(c[0][4], c[0][5], c[0][6], c[0][7]);
+        d0[0] = make_uint4(full[0][0], full[0][1], full[0][2], full[0][3]);
+        d0[1] = make_uint4(full[0][4], full[0][5], full[0][6], full[0][7]);
       } else {
 #pragma unroll
         for (int tt = 0; tt < kTerms; ++tt)
           *reinterpret_cast<uint4*>(dst + (size_t)tt * row_bytes + 16 * b) =
-              make_uint4(c[tt][0], c[tt][1], c[tt][2], c[tt][3]);
+              make_uint4(full[tt][0], full[tt][1], full[tt][2], full[tt][3]);
       }
       if (CHUNK) {  // tcgen05.cp chunks of 128-row tiles (many-rows path)
         const int m = r & 127;
@@ -429,6 +443,7 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
   }
   if (acc32) {
     const long n4 = (long)T * H / 4;
+    const long nthreads = (long)gridDim.x * blockDim.x;
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += nthreads)
       reinterpret_cast<float4*>(acc32)[i] = z;
@@ -521,8 +536,8 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
 cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
                                uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
                                float* row_w, int num_sms, cudaStream_t st) {
-  const long work = (long)T * (H / 32);
-  long blocks = (work + 127) / 128;
+  const long work = (long)T * (H / 32);  // 32-blocks, four threads each
+  long blocks = (work * 4 + 127) / 128;
   const long floor_blocks = ((long)T * H / 4 + 127) / 128;  // enough threads to zero acc32 quickly
   if (blocks < floor_blocks / 4) blocks = floor_blocks / 4;
   const long cap = (long)num_sms * 16;

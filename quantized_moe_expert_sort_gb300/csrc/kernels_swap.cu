@@ -76,14 +76,16 @@ template <> struct SwKind<SW_A4> {
 //   width and the swizzle span); kNS: operand stages; kSfRing: scale-chunk slots
 //   (a ring of its own, deeper than the operand ring); kSfLag: stages the scale
 //   warp's copies run ahead of its arrivals.
-// Packed e2m1 (mxf4) at stage 1 streams K = hidden in 128-byte rows (K tile 256).
-// At stage 2, K = inter is a few hundred (384 for the TP8 shard: 192 bytes per
-// row), so 128-byte boxes would leave half of every second box outside the
-// matrix; 64-byte rows (K tile 128, 64-byte swizzle) fit it exactly, and the
-// halved stages let twice as many be in flight, which this latency-bound short-K
-// stream needs. kind::mxf8f6f4 takes the weights expanded to one 16-element group
-// per 16 bytes (128-byte rows for a K tile of 128), so its tiles take twice the
-// shared memory per HBM byte.
+// Packed e2m1 (mxf4) streams K in 128-byte rows (K tile 256) at stage 1. At stage
+// 2 K = inter is a few hundred (384 for the TP8 shard: 192 bytes per row):
+// 128-byte boxes would leave half of every second box outside the matrix, and
+// with 42 KB stages only four fit, too few in flight for this short-item,
+// latency-bound stream. 64-byte rows (K tile 128, 64-byte swizzle) fit K exactly
+// and halve the stage, so nine are in flight (measured: TP8 a16w4 T = 64 stage 2
+// 140 -> 115 us).
+// kind::mxf8f6f4 takes the weights expanded to one 16-element group per 16 bytes
+// (128-byte rows for a K tile of 128), so its tiles take twice the shared memory
+// per HBM byte.
 template <int KIND, int STAGE> struct SwCfg {
   static constexpr bool kNarrow = SwKind<KIND>::kMxf4 && STAGE == 2;
   static constexpr int kKTile = SwKind<KIND>::kMxf4 && !kNarrow ? 256 : 128;
@@ -166,6 +168,39 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
   __syncwarp();
   return ok;
+}
+
+// Requantise one intermediate row y (lane = column j) per 32 along I: kTerms = 1
+// gives e4m3 (!kMxf4) or e2m1 codes with an e8m0 scale per block (MX rule); kTerms
+// > 1 carries the bf16-rounded y as kTerms e2m1 code terms, term t quantising
+// what the earlier terms left (exact residuals). Row r's term t is sub-row
+// r * kTerms + t of the codes (I / 2 bytes) and of the scales (os_stride bytes).
+template <int kTerms, bool kMxf4>
+__device__ __noinline__ void requant_row(float y, int row, int j, int lane, int I, uint8_t* oq, uint8_t* os,
+                                         int os_stride) {
+  if (kTerms > 1) y = __bfloat162float(__float2bfloat16_rn(y));
+#pragma unroll 1
+  for (int t = 0; t < kTerms; ++t) {
+    constexpr int emax = kMxf4 ? 2 : 8;
+    const float amax = warp_max(fabsf(y));
+    uint32_t sb = 127u;
+    float mul = 0.0f;
+    if (amax > 0.0f) {
+      int E = floor_log2_f32(amax) - emax;
+      E = E < -127 ? -127 : (E > 127 ? 127 : E);
+      sb = (uint32_t)(E + 127);
+      mul = exp2_neg(E);
+    }
+    if (kMxf4) {
+      const uint32_t code = cvt_e2m1x2(__fmul_rn(y, mul), 0.0f) & 0xFu;
+      const uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+      if ((lane & 1) == 0) oq[((size_t)row * kTerms + t) * (I / 2) + j / 2] = (uint8_t)(code | (nb << 4));
+      if (t + 1 < kTerms) y -= e2m1_to_f32(code) * e8m0_to_f32(sb);  // exact residual
+    } else {
+      oq[(size_t)row * I + j] = (uint8_t)(cvt_e4m3x2(__fmul_rn(y, mul), 0.0f) & 0xFFu);
+    }
+    if (lane == 0) os[((size_t)row * kTerms + t) * os_stride + j / 32] = (uint8_t)sb;
+  }
 }
 
 // Byte offset of (row m, block kb % 4) inside a 512-byte scale chunk.
@@ -320,11 +355,18 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
       tma_prefetch_desc(&tm_w);
       tma_prefetch_desc(&tm_x);
       const int sb_w = kdim / 32;
+      // Scale rows (weights and the item's sub-rows) are prefetched into L2 kPfAhead
+      // items ahead, so the scale warp's 4-byte copies do not pay the latency of
+      // HBM under the weight stream: one long stage-1 item covers it, short
+      // stage-2 items need several.
+      constexpr int kPfAhead = STAGE == 2 ? 4 : 1;
+      bool pf_end = false;
       auto prefetch_scales = [&](int j) {
+        if (pf_end) return;
         const int un = j % kURing;
-        if (!mbar_wait_or_abort(&ufull[un], (j / kURing) & 1, p.err, &abort_flag)) return;
+        if (!mbar_wait_or_abort(&ufull[un], (j / kURing) & 1, p.err, &abort_flag)) { pf_end = true; return; }
         const UItem nx = items[un];
-        if (nx.nrows < 0) return;
+        if (nx.nrows < 0) { pf_end = true; return; }  // no item is published past the end markers
         if (STAGE == 1) {
           const uint8_t* g = p.wscale + ((size_t)nx.e * 2 * I + (size_t)nx.tile * 128) * sb_w;
           bulk_prefetch_l2(g, 128u * sb_w);
@@ -333,8 +375,10 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
           const int rows = min(256, H - nx.tile * 256);
           bulk_prefetch_l2(p.wscale + ((size_t)nx.e * H + (size_t)nx.tile * 256) * sb_w, (uint32_t)rows * sb_w);
         }
+        const int nsub = nx.nrows * KD::kTerms;
+        bulk_prefetch_l2(p.as + (size_t)nx.row0 * KD::kTerms * p.xs_stride, (uint32_t)(nsub * p.xs_stride));
       };
-      prefetch_scales(0);
+      for (int j = 0; j < kPfAhead; ++j) prefetch_scales(j);
       uint32_t stage = 0;
       int it = 0;
       bool ok = true;
@@ -345,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
         mbar_arrive_relaxed(&uempty[us]);
         ++it;
         if (ui.nrows < 0) break;
-        prefetch_scales(it);
+        prefetch_scales(it + kPfAhead - 1);
         const int nsub = ui.nrows * KD::kTerms;  // B rows: the item's sub-rows
         const int nbox = (nsub + 15) / 16;
         const uint32_t btx = (uint32_t)nbox * 16 * C::kRow;
@@ -588,43 +632,21 @@ __global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p
       };
       if (STAGE == 1) {
         const int j = ui.tile * 128 + 32 * q + lane;  // intermediate column of this lane
+        // y = act(g, u) of item rows [c0, c0 + 16), requantised per 32 along I across the
+        // warp (one out-of-line call per row keeps this rarely repeated code small)
+        auto requant_rows = [&](int c0, const float* gv, const float* uv) {
+          const int nn = min(16, nrows - c0);
+#pragma unroll
+          for (int n = 0; n < 16; ++n)
+            if (n < nn)
+              requant_row<KD::kTerms, KD::kMxf4>(act_apply(p.act, gv[n], uv[n], p.beta, p.lbeta), row0 + c0 + n, j,
+                                                 lane, I, p.oq, p.os, p.os_stride);
+        };
         for (int c0 = 0; c0 < nrows; c0 += 16) {
           float gv[16], uv[16];
           load_pair(dg, dg + kAccCols, c0, gv, uv);
           release_acc(c0);
-          const int nn = min(16, nrows - c0);
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            if (n < nn) {
-              const int row = row0 + c0 + n;
-              float y = act_apply(p.act, gv[n], uv[n], p.beta, p.lbeta);
-              // A16: the bf16 intermediate; each code term quantises what the earlier ones left
-              if (KD::kTerms > 1) y = __bfloat162float(__float2bfloat16_rn(y));
-#pragma unroll
-              for (int t = 0; t < KD::kTerms; ++t) {
-                const int emax = KD::kMxf4 ? 2 : 8;
-                const float amax = warp_max(fabsf(y));
-                uint32_t sb = 127u;
-                float mul = 0.0f;
-                if (amax > 0.0f) {
-                  int E = floor_log2_f32(amax) - emax;
-                  E = E < -127 ? -127 : (E > 127 ? 127 : E);
-                  sb = (uint32_t)(E + 127);
-                  mul = exp2_neg(E);
-                }
-                if (KD::kMxf4) {
-                  const uint32_t code = cvt_e2m1x2(__fmul_rn(y, mul), 0.0f) & 0xFu;
-                  const uint32_t nb = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-                  if ((lane & 1) == 0)
-                    p.oq[((size_t)row * KD::kTerms + t) * (I / 2) + j / 2] = (uint8_t)(code | (nb << 4));
-                  if (t + 1 < KD::kTerms) y -= e2m1_to_f32(code) * e8m0_to_f32(sb);  // exact residual
-                } else {
-                  p.oq[(size_t)row * I + j] = (uint8_t)(cvt_e4m3x2(__fmul_rn(y, mul), 0.0f) & 0xFFu);
-                }
-                if (lane == 0) p.os[((size_t)row * KD::kTerms + t) * p.os_stride + j / 32] = (uint8_t)sb;
-              }
-            }
-          }
+          requant_rows(c0, gv, uv);
         }
       } else {
         const int h0 = ui.tile * 256 + 32 * q + lane;  // rows of H of this lane in tiles 0 and 1
@@ -665,6 +687,12 @@ template <int KIND, int STAGE>
 static cudaError_t set_limit_sw() {
   return cudaFuncSetAttribute(swap_stage_kernel<KIND, STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)SwLayout<KIND, STAGE>::total);
+}
+
+int swap_row_bytes(int kind, int stage) {
+  if (kind == SW_A16) return stage == 1 ? SwCfg<SW_A16, 1>::kRow : SwCfg<SW_A16, 2>::kRow;
+  if (kind == SW_A8) return stage == 1 ? SwCfg<SW_A8, 1>::kRow : SwCfg<SW_A8, 2>::kRow;
+  return stage == 1 ? SwCfg<SW_A4, 1>::kRow : SwCfg<SW_A4, 2>::kRow;
 }
 
 cudaError_t swap_set_smem_limits() {

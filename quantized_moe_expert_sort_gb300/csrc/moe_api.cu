@@ -415,14 +415,16 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   } else {
     ms = make_w13sw_map(c, w13, wkind);
     if (ms != MOE_OK) return ms;
-    // stage 2 streams K = inter: 64-byte rows for packed e2m1, 128-byte (unpacked) rows for A8
-    ms = adt == MOE_A_FP8 ? make_w2tc_map(c, w2, wkind) : make_w2sw_map(c, w2);
+    // stage 2 streams K = inter in the kernel's row width: 64-byte rows take the
+    // packed 64-byte-box map, 128-byte rows the 128-byte one (unpacked for A8)
+    const bool narrow2 = swap_row_bytes(swkind, 2) == 64;
+    ms = narrow2 ? make_w2sw_map(c, w2) : make_w2tc_map(c, w2, wkind);
     if (ms != MOE_OK) return ms;
     cuuint32_t box[2] = {128, 16};
-    cuuint32_t ibox[2] = {adt == MOE_A_FP8 ? 128u : 64u, 16};
+    cuuint32_t ibox[2] = {narrow2 ? 64u : 128u, 16};
     cuuint64_t idims[2] = {(cuuint64_t)i_row, (cuuint64_t)c->cap_rows * subs}, istr[1] = {(cuuint64_t)i_row};
     ms = encode(&tm_inter, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->inter_q, idims, istr, ibox,
-                adt == MOE_A_FP8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "intermediate rows");
+                narrow2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "intermediate rows");
     if (ms != MOE_OK) return ms;
     cuuint64_t xdims[2] = {(cuuint64_t)x_row, (cuuint64_t)c->cap_rows * subs}, xstr[1] = {(cuuint64_t)x_row};
     ms = encode(&tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->xq_sorted, xdims, xstr, box, CU_TENSOR_MAP_SWIZZLE_128B, "sorted activation rows");
@@ -483,13 +485,14 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     e = launch_tc_stage(kind, 2, p2, tm_inter, c->tm_w2tc, (int)(t2 < c->num_sms ? t2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   } else {
-    const long u1 = max_active * (c->I / 128), u2 = max_active * ((c->H + 255) / 256);
+    const long u2 = max_active * ((c->H + 255) / 256);
     StageParams q1 = p1;
     q1.aq = c->xq_sorted;
     q1.as = c->xs_sorted;
     q1.xs_stride = xs_sw;
     q1.os_stride = is_sw;
     prof_mark(c, st, "stage1");
+    const long u1 = max_active * (c->I / 128);
     e = launch_swap_stage(swkind, 1, q1, c->tm_w13sw, tm_xs, (int)(u1 < c->num_sms ? u1 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     StageParams q2 = p2;
@@ -497,7 +500,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q2.row_tok = c->row_tok;
     q2.row_w = c->row_w;
     prof_mark(c, st, "stage2");
-    e = launch_swap_stage(swkind, 2, q2, adt == MOE_A_FP8 ? c->tm_w2tc : c->tm_w2sw, tm_inter,
+    e = launch_swap_stage(swkind, 2, q2, swap_row_bytes(swkind, 2) == 64 ? c->tm_w2sw : c->tm_w2tc, tm_inter,
                           (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
