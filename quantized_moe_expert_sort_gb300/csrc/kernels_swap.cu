@@ -50,7 +50,8 @@
 namespace moe {
 namespace {
 
-constexpr int kThreadsSw = 384;
+// Threads per CTA: 4 role warps + one epilogue warpgroup (stage 1) or two (stage 2).
+template <int STAGE> constexpr int threads_sw() { return STAGE == 2 ? 384 : 256; }
 constexpr int kEpiWarpsSw = 4;  // warps per epilogue warpgroup; two warpgroups take alternate items
 
 template <int KIND> struct SwKind;
@@ -215,7 +216,7 @@ template <int KIND, int STAGE> constexpr uint32_t w_tile_tx() {
 }  // namespace
 
 template <int KIND, int STAGE>
-__global__ void __launch_bounds__(kThreadsSw, 1) swap_stage_kernel(StageParams p, const __grid_constant__ CUtensorMap tm_w,
+__global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(StageParams p, const __grid_constant__ CUtensorMap tm_w,
                                                                    const __grid_constant__ CUtensorMap tm_x) {
   using KD = SwKind<KIND>;
   using L = SwLayout<KIND, STAGE>;
@@ -709,9 +710,9 @@ template <int KIND>
 static cudaError_t launch_sw(int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                              int grid, cudaStream_t st) {
   if (stage == 1)
-    return launch_k(swap_stage_kernel<KIND, 1>, dim3(grid), dim3(kThreadsSw), SwLayout<KIND, 1>::total, st, true, p, tm_w,
+    return launch_k(swap_stage_kernel<KIND, 1>, dim3(grid), dim3(threads_sw<1>()), SwLayout<KIND, 1>::total, st, true, p, tm_w,
                     tm_x);
-  return launch_k(swap_stage_kernel<KIND, 2>, dim3(grid), dim3(kThreadsSw), SwLayout<KIND, 2>::total, st, true, p, tm_w,
+  return launch_k(swap_stage_kernel<KIND, 2>, dim3(grid), dim3(threads_sw<2>()), SwLayout<KIND, 2>::total, st, true, p, tm_w,
                   tm_x);
 }
 
