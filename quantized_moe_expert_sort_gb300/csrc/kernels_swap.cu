@@ -37,12 +37,14 @@
 //
 // CTA (one per SM, persistent): warp 3 enumerates the items (expert ids,
 // counts and offsets fetched 32 units at a time) and publishes them in a ring
-// in shared memory; warp 0 issues TMA for the weight tiles and the routed rows
-// (sorted rows are contiguous per expert: no gather); warp 1 copies the e8m0
-// scales of both operands with cp.async straight into the tcgen05.cp chunk
-// layout, two stages ahead of its mbarrier arrivals; warp 2 owns TMEM and
-// issues tcgen05.cp + tcgen05.mma; warps 4-7 run the epilogue from
-// double-buffered accumulators.
+// in shared memory (at stage 2 with each item's row tokens and top-k weights,
+// copied in by cp.async); warp 0 issues TMA for the weight tiles and the routed
+// rows (sorted rows are contiguous per expert: no gather) and prefetches scale
+// rows into L2; warp 1 copies the e8m0 scales of both operands with cp.async
+// straight into the tcgen05.cp chunk layout, kSfLag stages ahead of its
+// mbarrier arrivals; warp 2 owns TMEM and issues tcgen05.cp + tcgen05.mma;
+// warps 4-7 (stage 1) or 4-11 (stage 2: two warpgroups on alternate items) run
+// the epilogue from double-buffered accumulators.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
