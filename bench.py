@@ -205,6 +205,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# Dense tensor rate of the MMA kind each activation dtype runs on, relative to bf16
+# (nominal GB300 dense figures: bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s). bf16
+# activations run kind::mxf4 on five e2m1 code terms: 6 / 5 of the bf16 rate for
+# the algorithmic FLOPs.
+TENSOR_RATIO = {"bf16": 6.0 / 5.0, "fp8": 2.0, "fp4": 6.0}
+
+
+def tensor_peak_tflops(a_dtype):
+    """(peak TFLOP/s for the algorithmic FLOPs of a_dtype's MMA kind, source)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]) * TENSOR_RATIO[a_dtype], "measured bf16 burst x nominal kind ratio"
+    return 1900.0 * TENSOR_RATIO[a_dtype], "fallback bf16 burst x nominal kind ratio"
+
+
 def stored_traffic(config, kernel_name, T):
     """DRAM bytes per launch from a committed ncu summary, if it is current."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -325,8 +341,19 @@ def run_ours(args, world, rank, local, pg):
     ab = algo_bytes(args.tokens, n_active, n_pairs)
     dominant = max(("stage1", "stage2"), key=lambda k: per_avg.get(k, 0.0))
     peak, peak_kind = measured_peaks()
-    achieved = ab[dominant] / (per_avg[dominant] * 1e-3) / 1e9
+    tpeak, tpeak_kind = tensor_peak_tflops(CFG.a_dtype)
     flops = 6.0 * n_pairs * H * I
+    kflops = {"stage1": 4.0 * n_pairs * H * I, "stage2": 2.0 * n_pairs * H * I, "call": flops}
+    # the governing bound of a kernel: the slower of its bytes at the HBM peak and its
+    # FLOPs at the tensor peak of the MMA kind it runs
+    t_kernel = per_avg[dominant] * 1e-3
+    tensor_bound = kflops[dominant] / (tpeak * 1e12) > ab[dominant] / (peak * 1e9)
+    if tensor_bound:
+        achieved, kpeak, kunit, ksrc = kflops[dominant] / t_kernel / 1e12, tpeak, "TFLOP/s", tpeak_kind
+    else:
+        achieved, kpeak, kunit, ksrc = ab[dominant] / t_kernel / 1e9, peak, "GB/s", peak_kind
+    t_roof_call = max(ab["call"] / (peak * 1e9), flops / (tpeak * 1e12))
+    call_bound = "tensor" if flops / (tpeak * 1e12) > ab["call"] / (peak * 1e9) else "hbm"
     traffic = stored_traffic(args.config, dominant, args.tokens)
 
     # --- sweep over the decode token tiers
@@ -377,10 +404,13 @@ def run_ours(args, world, rank, local, pg):
                          "line is written back inside the step; both outside the events)",
                    "active_experts": n_active, "routed_pairs": n_pairs,
                    "sweep_us_per_call": sweep, "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
-                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "kernel": dominant,
+                     "achieved": round(achieved, 1), "peak": round(kpeak, 1), "peak_source": ksrc, "unit": kunit,
+                     "frac": round(achieved / kpeak, 4),
                      "traffic": traffic, "algo_bytes_per_launch": ab[dominant],
-                     "call_frac": round(ab["call"] / (step_ms * 1e-3) / 1e9 / peak, 4),
+                     "algo_flops_per_launch": kflops[dominant],
+                     "call_bound": call_bound,
+                     "call_frac": round(t_roof_call / (step_ms * 1e-3), 4),
                      "kernel_ms": {k: round(v, 5) for k, v in per_avg.items()}},
         "gpu_launches": 5 * args.steps,
         "clocks": clocks,
