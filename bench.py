@@ -412,7 +412,9 @@ def run_ours(args, world, rank, local, pg):
                      "call_bound": call_bound,
                      "call_frac": round(t_roof_call / (step_ms * 1e-3), 4),
                      "kernel_ms": {k: round(v, 5) for k, v in per_avg.items()}},
-        "gpu_launches": 5 * args.steps,
+        # sort (one kernel up to 8192 pairs, else histogram + scan + placement),
+        # activation scatter, stage 1, stage 2, finalize; per timed call
+        "gpu_launches": ((1 if args.tokens * K <= 8192 else 3) + 4) * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": args.tokens * H * 2 + args.tokens * K * 8,
