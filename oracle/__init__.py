@@ -55,6 +55,12 @@ def lib():
         L.orc_moe_dense.restype = i64
         L.orc_moe_dense.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                     i32, d, d, i32, vp, vp]
+        L.orc_activation_row.restype = None
+        L.orc_activation_row.argtypes = [vp, i32, i32, vp]
+        L.orc_requantize_intermediate.restype = None
+        L.orc_requantize_intermediate.argtypes = [vp, i32, i32, vp]
+        L.orc_route.restype = i64
+        L.orc_route.argtypes = [vp, i32, i32, i32, vp, vp]
         L.orc_num_threads.restype = i32
         L.orc_num_threads.argtypes = []
         _lib = L
@@ -197,6 +203,33 @@ def moe_dense(x_bf16, ids, w, w13, w13s, w2, w2s, act_kind, beta, lbeta, a_dtype
     if dropped < 0:
         raise ValueError("oracle rejected the arguments")
     return out_f64, out_bf16, int(dropped)
+
+
+def activation_row(x_bits_row, a_dtype):
+    """The stage-1 activation operand of one token (uint16 bf16 bits [H]) as float64 [H]."""
+    x = _c(x_bits_row, np.uint16).reshape(-1)
+    out = np.zeros(x.size, dtype=np.float64)
+    lib().orc_activation_row(_p(x), x.size, ADTYPE[a_dtype], _p(out))
+    return out
+
+
+def requantize_intermediate(y, a_dtype):
+    """One pair's stage-1 output y (float64 [I]) held in fp32 and requantised; float64 [I]."""
+    y = _c(y, np.float64).reshape(-1)
+    out = np.zeros(y.size, dtype=np.float64)
+    lib().orc_requantize_intermediate(_p(y), y.size, ADTYPE[a_dtype], _p(out))
+    return out
+
+
+def route(logits, K):
+    """Top-k softmax router: logits fp32 [T,E] -> (ids int32 [T,K], weights float64 [T,K])."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, K), dtype=np.int32)
+    w = np.zeros((T, K), dtype=np.float64)
+    if lib().orc_route(_p(logits), T, E, K, _p(ids), _p(w)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return ids, w
 
 
 def quantize_weights(w_f32):

@@ -248,7 +248,7 @@ double orc_act(int act, double g, double u, double beta, double lbeta) {
 /* The activation row the stage-1 GEMM sees: bf16 x as is (a16), or x
  * quantised to fp8 / fp4 with 1x32 e8m0 scales along H and dequantised
  * (a8 / a4; aiter PR 4463 "What"). */
-static void activation_row(const uint16_t* xrow, int H, int a_dtype, double* a) {
+void orc_activation_row(const uint16_t* xrow, int H, int a_dtype, double* a) {
     if (a_dtype == ORC_A_BF16) {
         for (int h = 0; h < H; ++h) a[h] = orc_bf16_value(xrow[h]);
         return;
@@ -265,7 +265,7 @@ static void activation_row(const uint16_t* xrow, int H, int a_dtype, double* a) 
 
 /* Stage-1 output held in fp32, then requantised: bf16 (a16) or fp8/fp4 1x32
  * along I (a8/a4; aiter PR 6259 Technical Details, PR 4463 item 2). */
-static void requantize_intermediate(const double* y, int I, int a_dtype, double* yq) {
+void orc_requantize_intermediate(const double* y, int I, int a_dtype, double* yq) {
     if (a_dtype == ORC_A_BF16) {
         for (int i = 0; i < I; ++i) yq[i] = orc_bf16_value(orc_bf16_from_f64((double)(float)y[i]));
         return;
@@ -333,7 +333,7 @@ int64_t orc_moe_forward(const uint16_t* x, const int32_t* ids, const float* w,
 #pragma omp parallel for schedule(dynamic)
         for (int i = 0; i < nsub; ++i) {
             int t = subset ? subset[i] : i;
-            activation_row(x + (size_t)t * H, H, a_dtype, a + (size_t)i * H);
+            orc_activation_row(x + (size_t)t * H, H, a_dtype, a + (size_t)i * H);
         }
 
         /* 2. stage 1 per block of sorted rows (one expert per block) */
@@ -365,7 +365,7 @@ int64_t orc_moe_forward(const uint16_t* x, const int32_t* ids, const float* w,
                     }
                 }
                 for (int q = 0; q < nr; ++q) {
-                    requantize_intermediate(y + (size_t)q * I, I, a_dtype, yq + (size_t)rows[q] * I);
+                    orc_requantize_intermediate(y + (size_t)q * I, I, a_dtype, yq + (size_t)rows[q] * I);
                     valid[rows[q]] = 1;
                 }
                 /* 3. stage 2 for the same rows */
@@ -439,7 +439,7 @@ int64_t orc_moe_dense(const uint16_t* x, const int32_t* ids, const float* w,
         double* y = (double*)malloc(sizeof(double) * (size_t)I);
         double* yq = (double*)malloc(sizeof(double) * (size_t)I);
         double* acc = (double*)calloc((size_t)H, sizeof(double));
-        activation_row(x + (size_t)t * H, H, a_dtype, a);
+        orc_activation_row(x + (size_t)t * H, H, a_dtype, a);
         for (int k = 0; k < K; ++k) {
             int e = ids[t * K + k];
             if (e < 0 || e >= E) continue;
@@ -455,7 +455,7 @@ int64_t orc_moe_dense(const uint16_t* x, const int32_t* ids, const float* w,
                 }
                 y[j] = orc_act(act, g, u, beta, lbeta);
             }
-            requantize_intermediate(y, I, a_dtype, yq);
+            orc_requantize_intermediate(y, I, a_dtype, yq);
             for (int h = 0; h < H; ++h) {
                 size_t row = (size_t)e * H + h;
                 double s = 0.0;
@@ -476,6 +476,46 @@ int64_t orc_moe_dense(const uint16_t* x, const int32_t* ids, const float* w,
         free(acc);
     }
     return dropped;
+}
+
+/* ---------------------------------------------------------------------------
+ * Top-k softmax router. The pages route every token to its top 16 experts
+ * (aiter PR 6259, Motivation: topk=16) but do not spell out the router; this is
+ * the plain reading used by the small parity workload: softmax over the E
+ * logits of a token, the K experts of largest probability, their probabilities
+ * renormalised to sum to one. Softmax is strictly increasing in the logit, so
+ * the K largest probabilities are the K largest logits; selecting on the logits
+ * keeps ties exact (equal logits: the lower expert id first) even where two
+ * probabilities would round to the same double. Selection order: descending
+ * logit, then ascending id.
+ * ------------------------------------------------------------------------- */
+int64_t orc_route(const float* logits, int T, int E, int K, int32_t* ids, double* weights) {
+    if (T < 0 || E <= 0 || K <= 0 || K > E) return -1;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        double* p = (double*)malloc(sizeof(double) * (size_t)E);
+        char* taken = (char*)calloc((size_t)E, 1);
+        double m = -INFINITY;
+        for (int e = 0; e < E; ++e) m = fmax(m, (double)l[e]);
+        double s = 0.0;
+        for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - m); s += p[e]; }
+        for (int e = 0; e < E; ++e) p[e] /= s;                 /* softmax over all E */
+        double sel = 0.0;
+        for (int k = 0; k < K; ++k) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;  /* strict: lower id wins ties */
+            taken[best] = 1;
+            ids[(size_t)t * K + k] = best;
+            weights[(size_t)t * K + k] = p[best];
+            sel += p[best];
+        }
+        for (int k = 0; k < K; ++k) weights[(size_t)t * K + k] /= sel;  /* renormalise over the K */
+        free(p);
+        free(taken);
+    }
+    return 0;
 }
 
 int orc_num_threads(void) {

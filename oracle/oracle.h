@@ -19,7 +19,7 @@
  *   - "Support SiTUv2 in the packed-int4 MoE stage1 epilogue" (aiter PR 4471),
  *     Motivation: y = silu(g)*u for SiLU; SiTUv2 applied in the stage-1 epilogue.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (the plain reading in each case):
  *   - MX scale rule: OCP MX, E = floor(log2(amax)) - emax_elem, clamped to
  *     [-127,127]; codes = RNE(v / 2^E) saturating; an all-zero block gets scale
  *     byte 127 and +0 codes.
@@ -80,6 +80,22 @@ int64_t orc_sort(const int32_t* ids, int T, int K, int E, int tile_m,
 /* y = act(g, u): SiLU  g*sigmoid(g)*u;
  *               SiTUv2 beta*tanh(g/beta)*sigmoid(g) * lbeta*tanh(u/lbeta). */
 double orc_act(int act, double g, double u, double beta, double lbeta);
+
+/* The stage-1 activation operand of one token: bf16 x as is (a16), or x
+ * quantised to fp8 / fp4 with 1x32 e8m0 scales along H and dequantised
+ * (a8 / a4). a receives H doubles. */
+void orc_activation_row(const uint16_t* xrow, int H, int a_dtype, double* a);
+
+/* The stage-1 output of one routed pair, y [I] (act(g, u) in fp64), held in
+ * fp32 and requantised: bf16 (a16) or fp8 / fp4 with 1x32 e8m0 scales along I
+ * (a8 / a4), dequantised into yq [I]. */
+void orc_requantize_intermediate(const double* y, int I, int a_dtype, double* yq);
+
+/* Top-k softmax router over E logits per token (fp32 [T,E], finite or -inf,
+ * at least one finite per token): ids [T,K] in descending logit order (equal
+ * logits: lower id first), weights [T,K] = the softmax probabilities of those
+ * experts renormalised over the K. Returns 0, or -1 on a bad argument. */
+int64_t orc_route(const float* logits, int T, int E, int K, int32_t* ids, double* weights);
 
 /* Whole forward pass, grouped by expert through orc_sort.
  * x bf16 [T,H]; ids int32 [T,K]; w fp32 [T,K];

@@ -82,16 +82,22 @@ def make_x(T: int, H: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.randn(T, H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+def make_router_logits(T: int, E: int, seed: int, device="cpu") -> torch.Tensor:
+    """Router logits ~ N(0, 1), fp32 [T, E]: the draw the "softmax_topk" routing starts from."""
+    g = _gen(seed, STREAM_ROUTING, 0, device)
+    return torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+
+
 def make_routing(T: int, E: int, K: int, kind: str, seed: int, zipf_s: float = 1.1, device="cpu"):
     """Returns (topk_ids int32 [T,K], topk_weights fp32 [T,K])."""
-    g = _gen(seed, STREAM_ROUTING, 0, device)
     if kind == "softmax_topk":
-        logits = torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+        logits = make_router_logits(T, E, seed, device)
         probs = torch.softmax(logits, dim=-1)
         order = torch.sort(-probs, dim=-1, stable=True).indices[:, :K]
         w = torch.gather(probs, 1, order)
         w = w / w.sum(dim=-1, keepdim=True)
         return order.to(torch.int32).contiguous(), w.to(torch.float32).contiguous()
+    g = _gen(seed, STREAM_ROUTING, 0, device)
     if kind == "uniform":
         keys = torch.rand(T, E, generator=g, device=device)
         ids = torch.sort(keys, dim=-1, stable=True).indices[:, :K]

@@ -3,9 +3,16 @@
 (1) the grouped (sort-driven) oracle equals the brute-force per-token loop;
 (2) identical experts reduce to one dense MLP scaled by the sum of the top-k
     weights; (3) E=1, K=1, w=1 equals a textbook dense MLP written with numpy
-    matrix products on weights decoded through the literal e2m1 table;
-(4) results do not depend on tile_m or on which tokens are evaluated;
-(5) dropped (out-of-range) pairs contribute nothing.
+    matrix products on weights decoded through the literal e2m1 table -- for
+    bf16 activations, and for fp8 / fp4 activations with x quantised per 32
+    along H and the fp32-held intermediate per 32 along I through the
+    separately pinned MX quantiser; each plausible mistake in that composition
+    (wrong quantisation axis, a quantisation step skipped) is shown to move
+    the result far outside the agreement the oracle reaches;
+(4) the fp32 holding of the intermediate before its requantisation, on values
+    built so that the fp32 rounding decides the code;
+(5) results do not depend on tile_m or on which tokens are evaluated;
+(6) dropped (out-of-range) pairs contribute nothing.
 """
 import numpy as np
 import pytest
@@ -92,6 +99,89 @@ def test_single_expert_is_textbook_mlp(act):
     assert np.max(np.abs(out - ref)) <= 1e-12 * np.max(np.abs(ref))
     ref16 = torch.tensor(ref).to(torch.float32).to(torch.bfloat16)  # ref is fp32-exact? check via bits
     assert np.mean(out16 == bf16_bits(ref16)) > 0.99
+
+
+FMT_OF = {"fp8": "e4m3", "fp4": "e2m1"}
+
+
+def _mx_roundtrip(v, adt):
+    """MX 1x32 quantise + dequantise along the last axis (the pinned quantiser)."""
+    c, sc = oracle.mx_quantize(np.ascontiguousarray(v, dtype=np.float64), FMT_OF[adt])
+    return oracle.mx_dequantize(c, sc, FMT_OF[adt])
+
+
+def _textbook(xf, W13, W2, act, adt, x_axis="H", y_axis="I", quant_x=True, quant_y=True, f32=True):
+    """Dense one-expert MLP in numpy; the keyword arguments plant the mistakes."""
+    I = W2.shape[1]
+    if quant_x:
+        a = _mx_roundtrip(xf, adt) if x_axis == "H" else _mx_roundtrip(xf.T, adt).T
+    else:
+        a = xf
+    gu = a @ W13.T
+    g, u = gu[:, :I], gu[:, I:]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    y = g * sig * u if act == "silu" else 4.0 * np.tanh(g / 4.0) * sig * 25.0 * np.tanh(u / 25.0)
+    if f32:
+        y = y.astype(np.float32).astype(np.float64)
+    if quant_y:
+        y = _mx_roundtrip(y, adt) if y_axis == "I" else _mx_roundtrip(y.T, adt).T
+    return y @ W2.T, y
+
+
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("adt", ["fp8", "fp4"])
+def test_single_expert_quantised_is_textbook_mlp(act, adt):
+    """a8w4 / a4w4: activations quantised 1x32 along H, the intermediate held in
+    fp32 and requantised 1x32 along I ("Add Kimi-K3 A8W4 support...", Technical
+    Details; "Add an opt-in a4w4 SiTUv2 MoE path...", What)."""
+    T = 32  # a multiple of 32, so that the wrong-axis mutations are well formed
+    c = make_case(T=T, E=1, K=1, seed=9)
+    w = np.ones((T, 1), np.float32)
+    ids = np.zeros((T, 1), np.int32)
+    out, _, inter, _ = oracle.moe_forward(c["x"], ids, w, c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                          act, 4.0, 25.0, adt, want_inter=True)
+    W13 = decode_fp4_ref(c["w13"][0], c["w13s"][0])
+    W2 = decode_fp4_ref(c["w2"][0], c["w2s"][0])
+    ref, yq = _textbook(c["xf"], W13, W2, act, adt)
+    assert np.array_equal(inter, yq)
+    scale = np.max(np.abs(ref))
+    assert np.max(np.abs(out - ref)) <= 1e-12 * scale
+    # each planted mistake lands far outside that 1e-12 agreement
+    for bad in (dict(x_axis="T"), dict(y_axis="T"), dict(quant_x=False), dict(quant_y=False)):
+        wrong, _ = _textbook(c["xf"], W13, W2, act, adt, **bad)
+        assert np.max(np.abs(out - wrong)) > 1e-3 * scale, bad
+
+
+@pytest.mark.parametrize("adt,big,tie,rounded,unrounded", [
+    # amax 4 -> e2m1 scale 2^0; 2.5 is the tie between 2 and 3 -> even code (2)
+    ("fp4", 4.0, 2.5 + 2.0 ** -40, 2.0, 3.0),
+    # amax 256 -> e4m3 scale 2^0; 1.0625 is the tie between 1 and 1.125 -> even (1)
+    ("fp8", 256.0, 1.0625 + 2.0 ** -40, 1.0, 1.125),
+    # bf16: 1 + 2^-8 is the tie between 1 and 1 + 2^-7 -> even (1)
+    ("bf16", 4.0, 1.0 + 2.0 ** -8 + 2.0 ** -40, 1.0, 1.0 + 2.0 ** -7),
+])
+def test_intermediate_is_held_in_fp32_before_requantisation(adt, big, tie, rounded, unrounded):
+    """The stage-1 output is rounded to fp32 before it is requantised: a value a
+    hair above a rounding tie becomes the tie in fp32 and then rounds to even."""
+    y = np.zeros(32)
+    y[0], y[1] = big, tie
+    yq = oracle.requantize_intermediate(y, adt)
+    assert yq[0] == big and yq[1] == rounded
+    # control: without the fp32 step the same value rounds the other way
+    if adt == "bf16":
+        direct = oracle.bf16_value(oracle.bf16_from_f64(tie))
+    else:
+        direct = _mx_roundtrip(y, adt)[1]
+    assert direct == unrounded
+
+
+@pytest.mark.parametrize("adt", ["fp8", "fp4"])
+def test_activation_row_is_the_block_roundtrip_along_h(adt):
+    c = make_case(T=3, H=256, seed=2)
+    for t in range(3):
+        a = oracle.activation_row(c["x"][t], adt)
+        assert np.array_equal(a, _mx_roundtrip(c["xf"][t], adt))
+    assert np.array_equal(oracle.activation_row(c["x"][0], "bf16"), c["xf"][0])
 
 
 def test_tile_m_and_subset_invariance():
