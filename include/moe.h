@@ -105,7 +105,7 @@ typedef struct {
  * inter_codes rows follow the sorted order of the last moe_forward (sort.tile_m
  * gives its padding: 1 on the few-rows tensor-core path, 128 on the many-rows
  * one); the element format follows its a_dtype: fp8 -> e4m3 bytes, fp4 -> e2m1
- * pairs, bf16 -> layout 2 below (five e2m1 code terms whose sum carries the bf16
+ * pairs, bf16 -> layout 2 below (a16_terms e2m1 code terms whose sum carries the bf16
  * intermediate). act_codes / act_scales hold per-token codes only after
  * moe_quantize_activations-style use; the forward writes activations straight
  * into sorted order. */
@@ -122,10 +122,20 @@ typedef struct {
                                  1: per 128-row tile b and 4-block chunk c, 512 bytes at
                                     (b * I/128 + c) * 512, byte 16*(m%32) + 4*(m/32) + kb%4
                                     for tile row m and 32-block kb (many-rows path);
-                                 2: five e2m1 code terms per value, term t of row r stored as
-                                    sub-row 5r + t: codes [5 rows, I/2] (two codes per byte),
-                                    scales [5 rows, inter_scale_stride]; value = sum of the five
-                                    terms */
+                                 2: a16_terms e2m1 code terms per value, term t of row r
+                                    stored as sub-row a16_terms * r + t: codes [a16_terms rows,
+                                    I/2] (two codes per byte), scales [a16_terms rows,
+                                    inter_scale_stride]; value = sum of the terms */
+  /* The stage-1 activation operand the last moe_forward wrote (x quantised per
+     32 along H) in the same sorted row order and with the same layout number as
+     the intermediate above (H in place of I): codes [rows, H * bytes/elt] (layout
+     2: [a16_terms rows, H/2]), scales as inter_scale_layout with
+     act_sorted_scale_stride bytes per (sub-)row (layouts 0 and 2). */
+  uint8_t* act_sorted_codes;
+  uint8_t* act_sorted_scales;
+  int32_t act_sorted_scale_stride;
+  int32_t a16_terms;          /* e2m1 code terms per bf16 value in layout 2 (each term's scale
+                                 by the MX rule on what the earlier terms left over) */
 } moe_workspace_view;
 
 /* Create a context on `device` for fixed (hidden, inter, num_experts, topk) and
@@ -148,8 +158,8 @@ moe_status moe_sort(moe_ctx* ctx, const int32_t* topk_ids, int num_tokens, int t
 /* Scratch of moe_sort_noalloc, in ints (a 1 MiB device array per GPU). */
 #define MOE_SORT_NOALLOC_SCRATCH_INTS 262144
 
-/* The expert sort of moe_sort, into buffers the caller passes, with no device
- * memory allocated by this call or by any set-up it needs. The aiter pages
+/* The expert sort of moe_sort, into buffers the caller passes; the call itself
+ * allocates no device memory. The aiter pages
  * have no counterpart: it serves callers of this library that cannot call
  * cudaMalloc -- a serving engine whose memory pool owns the GPU's memory, a
  * decode loop that must not risk the device synchronisation an allocation can
@@ -165,8 +175,11 @@ moe_status moe_sort(moe_ctx* ctx, const int32_t* topk_ids, int num_tokens, int t
  * problems are rejected with MOE_ERR_INVALID_ARG (use moe_sort). Every call
  * shares that array: calls whose kernels overlap on the GPU (different streams
  * without ordering, or several host threads) race and must be serialised by
- * the caller. The first call on a device looks up the array's device address
- * and sets kernel attributes; make that first call before any stream capture. */
+ * the caller. The first call on a device loads the library's module that holds
+ * the array (under lazy module loading this is when its 1 MiB is reserved,
+ * which can synchronise the device), looks up the array's device address and
+ * sets kernel attributes: make that first call at start-up, before any stream
+ * capture. */
 moe_status moe_sort_noalloc(const int32_t* topk_ids, int num_tokens, int topk, int num_experts, int tile_m,
                             int32_t* sorted_ids, int32_t* block_expert, int32_t* expert_count,
                             int32_t* expert_offset, int32_t* active_experts, int32_t* meta, void* stream);
@@ -206,6 +219,23 @@ moe_status moe_forward_host(moe_ctx* ctx, const void* x_host, const int32_t* top
 moe_status moe_quantize_activations(const void* x, int num_tokens, int hidden, int a_dtype, uint8_t* codes,
                                     uint8_t* scales, void* stream);
 
+/* Top-k softmax router (upstream of the expert computation). For each of the
+ * num_tokens rows of logits (device fp32 [T,E], finite or -inf, at least one
+ * finite per row; NaN is not allowed): softmax over the E logits, the topk
+ * experts of largest probability, their probabilities renormalised over the
+ * topk. The pages route every token to its top 16 of the global experts ("Add
+ * Kimi-K3 A8W4 support to the FlyDSL MegaMoE V2 operator", Motivation); the
+ * router arithmetic is the plain reading of that routing. Selection compares
+ * the logits exactly (softmax is increasing in the logit), in descending order,
+ * equal logits taking the lower expert id first; weights are computed in fp32
+ * as exp(l_k - l_max) / sum over the chosen of exp(l_j - l_max).
+ * Outputs (device, caller-owned): topk_ids int32 [T,K], topk_weights fp32 [T,K],
+ * both in selection order -- the layout moe_forward takes. Limits:
+ * 1 <= topk <= min(num_experts, 32), num_experts <= 4096; otherwise
+ * MOE_ERR_INVALID_ARG. Needs no context; enqueued on `stream`. */
+moe_status moe_route(const float* logits, int num_tokens, int num_experts, int topk, int32_t* topk_ids,
+                     float* topk_weights, void* stream);
+
 /* MXFP4 weight quantisation: fp32 w [rows, cols] (device, cols % 32 == 0) ->
  * e2m1 codes [rows, cols/2] + e8m0 scales [rows, cols/32] with the same rule.
  * Needs no context. */
@@ -231,6 +261,20 @@ moe_status moe_set_profiling(moe_ctx* ctx, int enable);
  * launch group: "sort", "act_quant", "stage1", "stage2", "finalize".
  * *count is the capacity on entry and the number written on return. */
 moe_status moe_read_profile(moe_ctx* ctx, float* ms, const char** names, int* count);
+
+/* Failure-detection support (no GPU fault is involved in either).
+ * moe_selftest_wait: one warp waits on a shared-memory barrier with the same
+ * bounded wait every pipeline stage uses, but with a limit of limit_ns
+ * (0 .. 1e10); complete != 0 completes the barrier first. A wait that runs out
+ * sets MOE_DEVERR_TIMEOUT in ctx's device error word and the kernel returns,
+ * so the next moe_get_error reports MOE_ERR_TIMEOUT and the context stays
+ * usable. Enqueued on `stream`.
+ * moe_debug_inject(MOE_INJECT_ALLOC_FAIL, n): the next moe_create (on any
+ * thread) treats its n-th workspace allocation (0-based) as failed: it frees
+ * what it had allocated and returns MOE_ERR_OOM. One-shot; n < 0 disarms. */
+#define MOE_INJECT_ALLOC_FAIL 1
+moe_status moe_selftest_wait(moe_ctx* ctx, int64_t limit_ns, int complete, void* stream);
+moe_status moe_debug_inject(int what, int64_t arg);
 
 /* Static text for a status. */
 const char* moe_status_string(moe_status s);

@@ -59,6 +59,8 @@ def lib():
         L.orc_activation_row.argtypes = [vp, i32, i32, vp]
         L.orc_requantize_intermediate.restype = None
         L.orc_requantize_intermediate.argtypes = [vp, i32, i32, vp]
+        L.orc_expert_stage1.restype = i64
+        L.orc_expert_stage1.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, d, d, i32, vp, vp]
         L.orc_route.restype = i64
         L.orc_route.argtypes = [vp, i32, i32, i32, vp, vp]
         L.orc_num_threads.restype = i32
@@ -219,6 +221,24 @@ def requantize_intermediate(y, a_dtype):
     out = np.zeros(y.size, dtype=np.float64)
     lib().orc_requantize_intermediate(_p(y), y.size, ADTYPE[a_dtype], _p(out))
     return out
+
+
+def expert_stage1(x_bits, tokens, w13e, w13se, act_kind, beta, lbeta, a_dtype):
+    """Stage 1 of one expert for token rows `tokens` of x (uint16 bf16 bits [T,H]);
+    w13e [2I,H/2], w13se [2I,H/32]. Returns (y32 [n,I], the fp32-held stage-1 output,
+    yq [n,I], the requantised intermediate)."""
+    x_bits = _c(x_bits, np.uint16)
+    tokens = _c(tokens, np.int32).reshape(-1)
+    H = x_bits.shape[1]
+    I = w13e.shape[0] // 2
+    n = tokens.size
+    y32 = np.zeros((n, I), dtype=np.float64)
+    yq = np.zeros((n, I), dtype=np.float64)
+    st = lib().orc_expert_stage1(_p(x_bits), _p(tokens), n, H, I, _p(_c(w13e, np.uint8)), _p(_c(w13se, np.uint8)),
+                                 ACT[act_kind], float(beta), float(lbeta), ADTYPE[a_dtype], _p(y32), _p(yq))
+    if st != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y32, yq
 
 
 def route(logits, K):

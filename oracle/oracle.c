@@ -478,6 +478,37 @@ int64_t orc_moe_dense(const uint16_t* x, const int32_t* ids, const float* w,
     return dropped;
 }
 
+/* Stage 1 of one expert for a list of token rows (the same steps as the grouped
+ * forward: activation operand, g and u against the expert's dequantised gate and
+ * up rows, act, fp32 holding, requantisation). */
+int64_t orc_expert_stage1(const uint16_t* x, const int32_t* tokens, int nrows, int H, int I,
+                          const uint8_t* w13e, const uint8_t* w13se, int act, double beta, double lbeta,
+                          int a_dtype, double* y32, double* yq) {
+    if (nrows < 0 || H <= 0 || I <= 0 || H % 32 || I % 32) return -1;
+    double* W = (double*)malloc(sizeof(double) * (size_t)2 * I * H); /* dequantised gate and up rows */
+    for (int j = 0; j < 2 * I; ++j)
+        weight_row(w13e + (size_t)j * (H / 2), w13se + (size_t)j * (H / 32), H, W + (size_t)j * H);
+#pragma omp parallel for schedule(dynamic)
+    for (int r = 0; r < nrows; ++r) {
+        double* a = (double*)malloc(sizeof(double) * (size_t)H);
+        double* y = (double*)malloc(sizeof(double) * (size_t)I);
+        orc_activation_row(x + (size_t)tokens[r] * H, H, a_dtype, a);
+        for (int j = 0; j < I; ++j) {
+            const double* wg = W + (size_t)j * H;
+            const double* wu = W + (size_t)(I + j) * H;
+            double g = 0.0, u = 0.0;
+            for (int h = 0; h < H; ++h) { g += a[h] * wg[h]; u += a[h] * wu[h]; }
+            y[j] = orc_act(act, g, u, beta, lbeta);
+            if (y32) y32[(size_t)r * I + j] = (double)(float)y[j];
+        }
+        orc_requantize_intermediate(y, I, a_dtype, yq + (size_t)r * I);
+        free(a);
+        free(y);
+    }
+    free(W);
+    return 0;
+}
+
 /* ---------------------------------------------------------------------------
  * Top-k softmax router. The pages route every token to its top 16 experts
  * (aiter PR 6259, Motivation: topk=16) but do not spell out the router; this is

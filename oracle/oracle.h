@@ -91,6 +91,15 @@ void orc_activation_row(const uint16_t* xrow, int H, int a_dtype, double* a);
  * (a8 / a4), dequantised into yq [I]. */
 void orc_requantize_intermediate(const double* y, int I, int a_dtype, double* yq);
 
+/* Stage 1 of one expert (w13e [2I, H/2] + w13se [2I, H/32]) for nrows token
+ * rows tokens[r] of x (bf16 [*, H]): y32 [nrows, I] (optional) receives the
+ * stage-1 output as held in fp32 before its requantisation, yq [nrows, I] the
+ * requantised intermediate -- the values orc_moe_forward produces for those
+ * pairs. Returns 0, or -1 on a bad argument. */
+int64_t orc_expert_stage1(const uint16_t* x, const int32_t* tokens, int nrows, int H, int I,
+                          const uint8_t* w13e, const uint8_t* w13se, int act, double beta, double lbeta,
+                          int a_dtype, double* y32, double* yq);
+
 /* Top-k softmax router over E logits per token (fp32 [T,E], finite or -inf,
  * at least one finite per token): ids [T,K] in descending logit order (equal
  * logits: lower id first), weights [T,K] = the softmax probabilities of those

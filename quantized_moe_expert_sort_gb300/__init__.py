@@ -17,6 +17,7 @@ ADTYPE = {"bf16": 0, "fp8": 1, "fp4": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "out of device memory",
           5: "expert id out of range", 6: "device wait timed out"}
 DEVERR_BAD_EXPERT, DEVERR_TIMEOUT, DEVERR_OVERFLOW = 1, 2, 4
+INJECT_ALLOC_FAIL = 1
 
 _lib = None
 
@@ -38,7 +39,9 @@ class _WorkspaceView(ctypes.Structure):
     _fields_ = [("sort", _SortView), ("act_codes", ctypes.c_void_p), ("act_scales", ctypes.c_void_p),
                 ("inter_codes", ctypes.c_void_p), ("inter_scales", ctypes.c_void_p), ("acc32", ctypes.c_void_p),
                 ("act_scale_stride", ctypes.c_int32), ("inter_scale_stride", ctypes.c_int32),
-                ("inter_scale_layout", ctypes.c_int32)]
+                ("inter_scale_layout", ctypes.c_int32), ("act_sorted_codes", ctypes.c_void_p),
+                ("act_sorted_scales", ctypes.c_void_p), ("act_sorted_scale_stride", ctypes.c_int32),
+                ("a16_terms", ctypes.c_int32)]
 
 
 def library_path():
@@ -61,6 +64,9 @@ def lib():
         L.moe_forward_host.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, f32, f32, i32, vp, vp]
         L.moe_quantize_activations.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_quantize_mxfp4.argtypes = [vp, i64, i32, vp, vp, vp]
+        L.moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.moe_selftest_wait.argtypes = [vp, i64, i32, vp]
+        L.moe_debug_inject.argtypes = [i32, i64]
         L.moe_get_workspace.argtypes = [vp, ctypes.POINTER(_WorkspaceView)]
         L.moe_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_set_profiling.argtypes = [vp, i32]
@@ -71,7 +77,8 @@ def lib():
         L.moe_last_error_message.restype = ctypes.c_char_p
         L.moe_last_error_message.argtypes = []
         for name in ("moe_create", "moe_destroy", "moe_sort", "moe_forward", "moe_forward_host",
-                     "moe_quantize_activations", "moe_quantize_mxfp4", "moe_get_workspace", "moe_get_error",
+                     "moe_quantize_activations", "moe_quantize_mxfp4", "moe_route", "moe_get_workspace",
+                     "moe_selftest_wait", "moe_debug_inject", "moe_get_error",
                      "moe_set_profiling", "moe_read_profile"):
             getattr(L, name).restype = i32
         _lib = L
@@ -204,24 +211,36 @@ class MoE:
         """Copies of the stage-1 output rows of the last forward: (codes, scales, fmt).
 
         fmt 'f16' / 'e4m3' / 'e2m1': codes [rows, I * bytes per element], scales [rows, I/32].
-        fmt 'e2m1x5' (bf16 activations on the tensor-core path): codes [rows, 5 I/2] and scales
-        [rows, 5 I/32], code term t in bytes [t I/2, (t+1) I/2) and scales [t I/32, (t+1) I/32);
-        value = sum of the five terms.
+        fmt 'e2m1xN' (bf16 activations on the few-rows path, N code terms): codes [rows, N I/2]
+        and scales [rows, N I/32], code term t in bytes [t I/2, (t+1) I/2) and scales
+        [t I/32, (t+1) I/32); value = sum of the N terms.
         """
         v = self.workspace()
-        if v.inter_scale_layout == 2:  # sub-row r * 5 + t holds code term t of row r
-            codes = _view(v.inter_codes, (rows, 5 * self.I // 2), torch.uint8).clone()
-            scales = _view(v.inter_scales, (rows * 5, v.inter_scale_stride), torch.uint8)[:, :self.I // 32]
-            return codes, scales.reshape(rows, 5 * self.I // 32).clone(), "e2m1x5"
+        return self._sorted_rows(v.inter_codes, v.inter_scales, v.inter_scale_stride, v.inter_scale_layout, rows,
+                                 self.I, a_dtype, v.a16_terms)
+
+    def sorted_activations(self, rows, a_dtype):
+        """Copies of the stage-1 activation operand rows the last forward wrote (x quantised
+        per 32 along H, in sorted order): (codes, scales, fmt) with the conventions of
+        intermediate(), H in place of I."""
+        v = self.workspace()
+        return self._sorted_rows(v.act_sorted_codes, v.act_sorted_scales, v.act_sorted_scale_stride,
+                                 v.inter_scale_layout, rows, self.H, a_dtype, v.a16_terms)
+
+    def _sorted_rows(self, codes_p, scales_p, stride, layout, rows, width, a_dtype, terms):
+        if layout == 2:  # sub-row r * terms + t holds code term t of row r
+            codes = _view(codes_p, (rows, terms * width // 2), torch.uint8).clone()
+            scales = _view(scales_p, (rows * terms, stride), torch.uint8)[:, :width // 32]
+            return codes, scales.reshape(rows, terms * width // 32).clone(), "e2m1x%d" % terms
         bpe = {"bf16": 2, "fp8": 1, "fp4": 0.5}[a_dtype]
         fmt = {"bf16": "f16", "fp8": "e4m3", "fp4": "e2m1"}[a_dtype]
-        codes = _view(v.inter_codes, (rows, int(self.I * bpe)), torch.uint8).clone()
-        if v.inter_scale_layout == 0:
-            scales = _view(v.inter_scales, (rows, v.inter_scale_stride), torch.uint8)[:, :self.I // 32].clone()
+        codes = _view(codes_p, (rows, int(width * bpe)), torch.uint8).clone()
+        if layout == 0:
+            scales = _view(scales_p, (rows, stride), torch.uint8)[:, :width // 32].clone()
         else:  # 128-row tiles of 512-byte chunks (tensor-core path)
-            nb, nc = rows // 128, self.I // 128
-            raw = _view(v.inter_scales, (nb, nc, 32, 4, 4), torch.uint8)  # [tile, chunk, m%32, m/32, kb%4]
-            scales = raw.permute(0, 3, 2, 1, 4).reshape(rows, self.I // 32).clone()
+            nb, nc = rows // 128, width // 128
+            raw = _view(scales_p, (nb, nc, 32, 4, 4), torch.uint8)  # [tile, chunk, m%32, m/32, kb%4]
+            scales = raw.permute(0, 3, 2, 1, 4).reshape(rows, width // 32).clone()
         return codes, scales, fmt
 
     def set_profiling(self, enable=True):
@@ -234,6 +253,10 @@ class MoE:
         n = ctypes.c_int(8)
         _check(lib().moe_read_profile(self._h, ms, names, ctypes.byref(n)))
         return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+    def selftest_wait(self, limit_ns, complete, stream=None):
+        """Run the bounded-wait self-test kernel (see moe_selftest_wait)."""
+        _check(lib().moe_selftest_wait(self._h, int(limit_ns), 1 if complete else 0, _stream(stream)))
 
     def get_error(self):
         """(status, device flag bits); reading clears the device error word."""
@@ -256,6 +279,21 @@ def quantize_activations(x, a_dtype, stream=None):
     _check(lib().moe_quantize_activations(_ptr(x), T, H, ADTYPE[a_dtype], _ptr(codes), _ptr(scales),
                                           _stream(stream)))
     return codes, scales
+
+
+def debug_inject_alloc_failure(n):
+    """The next context creation fails its n-th workspace allocation (MOE_ERR_OOM); n < 0 disarms."""
+    _check(lib().moe_debug_inject(INJECT_ALLOC_FAIL, int(n)))
+
+
+def route(logits, topk, stream=None):
+    """Top-k softmax router on the GPU: logits fp32 [T,E] -> (topk_ids int32 [T,K], topk_weights fp32 [T,K])."""
+    _require(logits, torch.float32, "logits")
+    T, E = logits.shape
+    ids = torch.empty((T, topk), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, topk), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route(_ptr(logits), T, E, topk, _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
 
 
 def quantize_mxfp4(w, stream=None):

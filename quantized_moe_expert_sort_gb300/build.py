@@ -9,7 +9,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "kernels_prep.cu", "kernels_tc.cu", "kernels_swap.cu", "sort_noalloc.cu"]
+SOURCES = ["moe_api.cu", "kernels_prep.cu", "kernels_tc.cu", "kernels_swap.cu", "kernels_route.cu",
+           "sort_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -3,12 +3,14 @@
 // Formats follow the OCP MX definitions used on the aiter pages ("Add an opt-in
 // a4w4 SiTUv2 MoE path...", Three tuner defects item 2: fp4x2 packs two e2m1
 // codes per byte; "Add Kimi-K3 A8W4 support...", Technical Details: fp8 1x32
-// block scales). Activation operands of both GEMMs are "block-scaled codes":
-// a code array plus one e8m0 scale per 32 elements along K, with codes in one
-// of three element formats:
-//   FMT_F16  : IEEE half (the lossless re-encoding of bf16 values, a16 path)
+// block scales). Quantised activations are "block-scaled codes": a code array
+// plus one e8m0 scale per 32 elements along K, with codes in one of the formats:
 //   FMT_E4M3 : fp8 e4m3fn (a8 path)
-//   FMT_E2M1 : fp4 e2m1, two per byte, element 2j in the low nibble (a4 path)
+//   FMT_E2M1 : fp4 e2m1, two per byte, element 2j in the low nibble (a4 path;
+//              also the code terms that carry bf16 values on the a16 path)
+//   FMT_F16  : IEEE half times one power of two per token: the bf16 mode of the
+//              stand-alone activation quantiser (moe_quantize_activations) only;
+//              the forward pass does not use it
 #pragma once
 
 #include <cstdint>
@@ -91,9 +93,11 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
 
 // ---------------------------------------------------------------------------
 // Activation functions (aiter PR 6259 Motivation, PR 4471 Motivation)
-// sigmoid(z) = 1 / (1 + 2^(-z * log2 e)) with the hardware exp2 and reciprocal;
-// tanh(z) = 2 * sigmoid(2z) - 1, the identity the int4 SiTUv2 page builds tanh
-// from: it saturates to +-1 at both ends without clamping.
+// sigmoid(z) = 1 / (1 + 2^(-z * log2 e)) with the hardware exp2 and reciprocal
+// (no cancellation: a few ulp). tanh is CUDA's tanhf: the int4 SiTUv2 page
+// builds tanh as 2 * sigmoid(2z) - 1, which in fp32 cancels for small z (up to
+// ~4e-4 relative at the |u| / linear_beta of small activations); tanhf keeps the
+// relative error at a few ulp and still saturates to exactly +-1 for large |z|.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float fast_sigmoid(float z) {
   float e, r;
@@ -102,13 +106,11 @@ __device__ __forceinline__ float fast_sigmoid(float z) {
   return r;
 }
 
-__device__ __forceinline__ float fast_tanh(float z) { return 2.0f * fast_sigmoid(2.0f * z) - 1.0f; }
-
 __device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta) {
   const float sig = fast_sigmoid(g);
   if (act == ACT_SILU) return g * sig * u;
-  const float situ = beta * fast_tanh(g / beta) * sig;
-  const float up = lbeta * fast_tanh(u / lbeta);
+  const float situ = beta * tanhf(g / beta) * sig;
+  const float up = lbeta * tanhf(u / lbeta);
   return situ * up;
 }
 
@@ -233,15 +235,20 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// Bounded wait with an explicit wall-clock limit (ns).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int* err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait_suspend(bar, parity, MOE_SUSPEND_NS)) return true;
-    if (global_ns() - t0 > MOE_WAIT_NS) break;
+    if (global_ns() - t0 > limit_ns) break;
   }
   set_error(err, DEV_ERR_TIMEOUT);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait_limit(bar, parity, err, MOE_WAIT_NS);
 }
 
 // Wait that drains instead of hanging: once any thread of the CTA has timed

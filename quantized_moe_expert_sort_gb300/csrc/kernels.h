@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cuda.h>
 
 namespace moe {
@@ -47,6 +48,7 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 size_t sort_small_smem(int E);
+size_t sort_scatter_smem(int E, long n);  // dynamic shared memory of the fused sort + scatter
 // Text returned by moe_last_error_message() on this thread.
 void set_last_error_message(const char* msg);
 cudaError_t prep_set_smem_limits();
@@ -58,19 +60,45 @@ cudaError_t launch_weight_quant(const float* w, long nblocks, uint8_t* codes, ui
                                 cudaStream_t st);
 cudaError_t launch_finalize(const float* acc32, long n, void* out, int num_sms, cudaStream_t st);
 // Activation quantisation for the tensor-core paths: each token's row is
-// quantised once (one thread per 32-block) and written straight to the sorted
+// quantised once (four threads per 32-block) and written straight to the sorted
 // rows of its routed pairs, codes [rows, row_bytes] and e8m0 scales
-// [rows, scale_stride], both row-major. mode SW_A8: e4m3; SW_A4: e2m1;
+// [rows, sstride], both row-major. mode SW_A8: e4m3; SW_A4: e2m1;
 // SW_A16: A16_TERMS e2m1 terms whose sum carries the bf16 value, term t of
 // sorted row r stored as sub-row r * A16_TERMS + t (codes [sub-rows, H/2],
-// scales [sub-rows, scale_stride]).
-// scale_stride 0 (SW_A8 / SW_A4 only): scales go to the 512-byte tcgen05.cp
+// scales [sub-rows, sstride]).
+// sstride 0 (SW_A8 / SW_A4 only): scales go to the 512-byte tcgen05.cp
 // chunks of 128-row tiles instead (byte 16*(m%32) + 4*(m/32) + b%4 of chunk
 // (r/128) * H/128 + b/4 for sorted row r, m = r % 128, 32-block b).
-// row_tok / row_w (optional): token and top-k weight of every sorted row.
-cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
-                               uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
-                               float* row_w, int num_sms, cudaStream_t st);
+struct ScatterOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  int sstride;
+  float* acc32;         // fp32 combine buffer [T,H], zeroed (nullptr: untouched)
+  const float* topk_w;  // row_tok / row_w (optional): token and top-k weight of every sorted row
+  int32_t* row_tok;
+  float* row_w;
+  int* tok_cnt;         // stage-2 arrival counters [T][nsl][4] (finalize inside stage 2), or nullptr;
+  int nsl;              // set to the token's number of routed pairs; nsl = 256-row slices of H
+  __nv_bfloat16* out;   // with tok_cnt: rows of tokens without a routed pair are zeroed here
+};
+cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row,
+                               const ScatterOut& so, int num_sms, cudaStream_t st);
+// The single-CTA sort and the scatter above in one launch (n <= SORT_SMALL_MAX_PAIRS):
+// every CTA sorts in shared memory, CTA 0 writes the sort outputs.
+cudaError_t launch_sort_scatter(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* err,
+                                const void* x, int T, int H, int K, int mode, const ScatterOut& sc, int num_sms,
+                                cudaStream_t st);
+
+// One warp waits on an mbarrier with a limit of limit_ns (complete != 0: the
+// barrier completes first); a wait that runs out sets DEV_ERR_TIMEOUT in *err.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int complete, int* err, cudaStream_t st);
+
+// Top-k softmax router over E logits per token (kernels_route.cu).
+constexpr int ROUTE_MAX_EXPERTS = 4096;
+constexpr int ROUTE_MAX_TOPK = 32;
+cudaError_t route_set_smem_limits();
+cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, int num_sms,
+                         cudaStream_t st);
 
 // Parameters of the grouped stage kernels.
 struct StageParams {
@@ -95,8 +123,17 @@ struct StageParams {
   const float* row_w;      // few-rows path: top-k weight of each sorted row
   const int4* active_info; // few-rows path: {expert, count, first row, 0} per active expert
   int xs_stride;       // bytes per row of the activation-scale array (as)
-  int aq_stride;       // bytes per row of the activation-code array (few-rows tensor-core path)
   int os_stride;       // stage 1: bytes per row of the output-scale array (os)
+  int tile_group;      // many-rows stage 2: N tiles per group of the tile order (<= 0: block-major)
+  // few-rows stage 2 with the finalize folded in (tok_cnt != nullptr): arrival counters
+  // [T][nsl][4] per (token, 256-row slice of H, 32-row quadrant), set by the scatter to
+  // the token's routed pairs; the warp that brings one to zero writes that part of out
+  int* tok_cnt;
+  int nsl;
+  __nv_bfloat16* out;
+  // few-rows kernels: 1 when the sort finished before the preceding kernel began, so the
+  // active-expert list may be read, and the weights loaded, before the wait on that kernel
+  int early_weights;
   int T, H, I, E, K;
   int act;
   float beta, lbeta;
@@ -119,7 +156,7 @@ cudaError_t launch_tc_stage(int kind, int stage, const TcParams& p, const CUtens
 // tcgen05 family for few routed rows per expert (decode): the weight tile is
 // the M = 128 operand and the expert's routed rows the N <= 64 operand.
 enum { SW_A16 = 0, SW_A8 = 1, SW_A4 = 2 };
-constexpr int A16_TERMS = 5;  // e2m1 code terms carrying one bf16 value (few-rows path)
+constexpr int A16_TERMS = 6;  // e2m1 code terms carrying one bf16 value (few-rows path)
 cudaError_t swap_set_smem_limits();
 // Shared-memory bytes per operand row (TMA box width) of the few-rows kernels'
 // (kind, stage): the tensor maps the host encodes must use this box width.

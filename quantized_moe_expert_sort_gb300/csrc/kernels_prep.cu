@@ -91,6 +91,20 @@ __device__ void sort_scan_and_fill(const int* cnt, int* cursor, int E, int tile_
   }
 }
 
+// The padded per-expert offsets alone (cursor[e] = first row of e), in shared memory.
+__device__ void sort_scan_offsets(const int* cnt, int* cursor, int E, int tile_m, int* scan_smem) {
+  int per = (E + blockDim.x - 1) / blockDim.x;
+  int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int rows = 0;
+  for (int e = e0; e < e1; ++e) rows += (cnt[e] + tile_m - 1) / tile_m * tile_m;
+  int total_rows;
+  int off = block_exclusive_scan(rows, scan_smem, &total_rows);
+  for (int e = e0; e < e1; ++e) {
+    cursor[e] = off;
+    off += (cnt[e] + tile_m - 1) / tile_m * tile_m;
+  }
+}
+
 // Stable placement of pairs [p0, p1) given cursor[e] = first free row of e.
 // Chunks of blockDim.x pairs in ascending order; inside a chunk the rank of a
 // pair among equal experts is (pairs of earlier warps, from a per-expert byte
@@ -127,7 +141,7 @@ __device__ void sort_place_range(const int32_t* ids, long p0, long p1, int E, in
         }
       }
       const int pos = cursor[e] + prefix + rank;
-      sorted_ids[pos] = (int32_t)p;
+      if (sorted_ids) sorted_ids[pos] = (int32_t)p;
       if (pair_row) pair_row[p] = pos;
     } else if (pair_row && p < p1) {
       pair_row[p] = -1;
@@ -338,16 +352,11 @@ __device__ __forceinline__ uint32_t block_scale_of(float amax, int emax, float* 
 // sorted rows of the token's K routed pairs (see launch_act_scatter). A16: A16_TERMS e2m1
 // terms per value, term t quantising (MX rule) what terms 0..t-1 left over (in
 // fp32 the residual v - code * 2^E is exact), term t of sorted row r written as
-// sub-row r * A16_TERMS + t.
+// sub-row r * A16_TERMS + t. Work units (token, 32-block) are taken 8 per warp
+// and pass by warps gw0, gw0 + nw, ...; pair_row may live in shared memory.
 template <int MODE, bool CHUNK>
-__global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
-                                                          const int32_t* __restrict__ pair_row,
-                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                          int sstride, float* __restrict__ acc32,
-                                                          const float* __restrict__ topk_w, int32_t* __restrict__ row_tok,
-                                                          float* __restrict__ row_w) {
-  pdl_wait();  // the sort's pair rows
-  pdl_launch_dependents();
+__device__ __forceinline__ void scatter_units(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+                                              const int32_t* pair_row, const ScatterOut& so, long gw0, long nw) {
   // Four threads (a quad of lanes) per (token, 32-block): thread q holds elements
   // 8q..8q+7, the block maximum is reduced across the quad, and the quad's threads
   // take the top-k destinations k = q, q + 4, ... (each writes the whole block).
@@ -357,9 +366,8 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
   const long total = (long)T * nb;
   const long row_bytes = MODE == SW_A8 ? (long)H : H / 2;  // one (sub-)row
   const int lane = threadIdx.x & 31, q = lane & 3, qbase = lane & ~3;
-  const long warps = (long)gridDim.x * (blockDim.x / 32);
   // warp-uniform loop: 8 blocks per warp and pass, every lane runs every pass
-  for (long w0 = ((long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * 8; w0 < total; w0 += warps * 8) {
+  for (long w0 = gw0 * 8; w0 < total; w0 += nw * 8) {
     const long w = w0 + (lane >> 2);
     const bool valid = w < total;
     const long t = valid ? w / nb : 0;
@@ -415,13 +423,13 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
         for (int i = 0; i < kWords; ++i) full[tt][kWords * s + i] = __shfl_sync(0xFFFFFFFFu, c[tt][i], qbase + s);
     if (!valid) continue;
     for (int k = q; k < K; k += 4) {
-      const int r = __ldg(pair_row + t * K + k);
+      const int r = pair_row[t * K + k];
       if (r < 0) continue;
-      if (row_tok && b == 0) {
-        row_tok[r] = (int32_t)t;
-        row_w[r] = __ldg(topk_w + t * K + k);
+      if (so.row_tok && b == 0) {
+        so.row_tok[r] = (int32_t)t;
+        so.row_w[r] = __ldg(so.topk_w + t * K + k);
       }
-      uint8_t* dst = codes + (size_t)r * kTerms * row_bytes;
+      uint8_t* dst = so.codes + (size_t)r * kTerms * row_bytes;
       if (MODE == SW_A8) {
         uint4* d0 = reinterpret_cast<uint4*>(dst + 32 * b);
         d0[0] = make_uint4(full[0][0], full[0][1], full[0][2], full[0][3]);
@@ -434,20 +442,119 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
       }
       if (CHUNK) {  // tcgen05.cp chunks of 128-row tiles (many-rows path)
         const int m = r & 127;
-        scales[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (m & 31) + 4 * (m >> 5) + (b & 3)] = (uint8_t)sc[0];
+        so.scales[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (m & 31) + 4 * (m >> 5) + (b & 3)] =
+            (uint8_t)sc[0];
       } else {
 #pragma unroll
-        for (int tt = 0; tt < kTerms; ++tt) scales[((size_t)r * kTerms + tt) * sstride + b] = (uint8_t)sc[tt];
+        for (int tt = 0; tt < kTerms; ++tt) so.scales[((size_t)r * kTerms + tt) * so.sstride + b] = (uint8_t)sc[tt];
       }
     }
   }
-  if (acc32) {
+}
+
+// Zero the fp32 combine buffer; set the stage-2 arrival counters of each token
+// to its number of routed pairs (the stage-2 warp that brings a counter to zero
+// writes the token's bf16 row) and write zeros for tokens with none.
+__device__ __forceinline__ void scatter_tail(int T, int H, int K, const int32_t* pair_row, const ScatterOut& so,
+                                             long tid0, long nthreads) {
+  if (so.acc32) {
     const long n4 = (long)T * H / 4;
-    const long nthreads = (long)gridDim.x * blockDim.x;
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += nthreads)
-      reinterpret_cast<float4*>(acc32)[i] = z;
+    for (long i = tid0; i < n4; i += nthreads) reinterpret_cast<float4*>(so.acc32)[i] = z;
   }
+  if (so.tok_cnt) {
+    for (long t = tid0; t < T; t += nthreads) {
+      int n = 0;
+      for (int k = 0; k < K; ++k) n += pair_row[t * K + k] >= 0;
+      int* cnt = so.tok_cnt + t * so.nsl * 4;
+      for (int i = 0; i < so.nsl * 4; ++i) cnt[i] = n;
+      if (n == 0) {
+        uint4* o = reinterpret_cast<uint4*>(so.out + t * H);
+        for (int i = 0; i < H / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+}
+
+template <int MODE, bool CHUNK>
+__global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int K,
+                                                          const int32_t* __restrict__ pair_row, ScatterOut so) {
+  pdl_wait();  // the sort's pair rows
+  pdl_launch_dependents();
+  scatter_units<MODE, CHUNK>(x, T, H, K, pair_row, so, (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5),
+                             (long)gridDim.x * (blockDim.x / 32));
+  scatter_tail(T, H, K, pair_row, so, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
+}
+
+// L2 prefetch of a contiguous range (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// The sort and the activation scatter in one launch, for up to
+// SORT_SMALL_MAX_PAIRS pairs ("Add an opt-in a4w4 SiTUv2 MoE path...", Three
+// tuner defects item 2: a separate quant kernel costs a launch at small token
+// counts). Every CTA sorts all pairs in shared memory (the same histogram, scan
+// and stable placement as sort_small_kernel: identical results in every CTA),
+// CTA 0 publishes the sort, and each CTA then quantises its share of the
+// (token, 32-block) units straight into the sorted rows, reading each pair's
+// row from its own shared-memory copy. Each CTA first pulls its share of x into
+// L2, so that load overlaps the sort.
+template <int MODE, bool CHUNK>
+__global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int tile_m,
+                                                            SortOut so, int* err, const __nv_bfloat16* __restrict__ x,
+                                                            int T, int H, int K, ScatterOut sc) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int* cnt = reinterpret_cast<int*>(smem);                     // [E]
+  int* cursor = cnt + E;                                       // [E]
+  int* scan_smem = cursor + E;                                 // [32]
+  int32_t* prow = scan_smem + 32;                              // [n]
+  uint8_t* wtab = reinterpret_cast<uint8_t*>(prow + ((n + 3) & ~3));  // [E][32]
+  const bool lead = blockIdx.x == 0;
+  {  // this CTA's share of x, into L2 ahead of the scatter (4 KB pieces)
+    const long xb = (long)T * H * 2;
+    for (long o = ((long)blockIdx.x * blockDim.x + threadIdx.x) * 4096; o < xb;
+         o += (long)gridDim.x * blockDim.x * 4096)
+      prefetch_l2(reinterpret_cast<const uint8_t*>(x) + o, (uint32_t)min(4096L, xb - o));
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  if (n >= E) {
+    for (int i = threadIdx.x; i < E * 8; i += blockDim.x) reinterpret_cast<uint32_t*>(wtab)[i] = 0u;
+  } else {  // few pairs: clear only the table rows of experts that occur
+    for (int p = threadIdx.x; p < n; p += blockDim.x) {
+      const int e = ids[p];
+      if (e >= 0 && e < E) {
+        uint4* row = reinterpret_cast<uint4*>(wtab + e * 32);
+        row[0] = make_uint4(0u, 0u, 0u, 0u);
+        row[1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int p = threadIdx.x; p < n; p += blockDim.x) {
+    int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad && lead) set_error(err, DEV_ERR_BAD_EXPERT);
+  __syncthreads();
+  // only CTA 0 writes the sort's global outputs; the others keep offsets in shared memory
+  if (lead) {
+    sort_scan_and_fill(cnt, cursor, E, tile_m, n, so, scan_smem);
+  } else {
+    sort_scan_offsets(cnt, cursor, E, tile_m, scan_smem);
+  }
+  __syncthreads();
+  sort_place_range(ids, 0, n, E, cursor, wtab, lead ? so.sorted_ids : nullptr, prow);
+  __syncthreads();
+  if (lead && so.pair_row)
+    for (int p = threadIdx.x; p < n; p += blockDim.x) so.pair_row[p] = prow[p];
+  // the dependent kernel may launch now; it waits for this grid's completion
+  pdl_launch_dependents();
+  scatter_units<MODE, CHUNK>(x, T, H, K, prow, sc, (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5),
+                             (long)gridDim.x * (blockDim.x / 32));
+  scatter_tail(T, H, K, prow, sc, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
 }
 
 // MXFP4 weight quantisation: fp32 [rows, cols] -> e2m1 codes [rows, cols/2] +
@@ -479,9 +586,29 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
   }
 }
 
+// Self-test of the bounded wait every pipeline uses: one warp waits on an
+// mbarrier that is completed first (complete != 0) or never, with a wall-clock
+// limit; a wait that runs out sets DEV_ERR_TIMEOUT and the kernel returns.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint64_t limit_ns, int complete, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && complete) mbar_arrive(&bar);
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, err, limit_ns);
+}
+
 // ---------------------------------------------------------------------------
 // Host-side launchers
 // ---------------------------------------------------------------------------
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int complete, int* err, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, complete, err);
+  return cudaGetLastError();
+}
+
 size_t sort_small_smem(int E) { return (size_t)E * 8 + 32 * 4 + (size_t)E * 32; }
 
 cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* hist, int hist_cap_chunks,
@@ -503,10 +630,21 @@ cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const Sor
   return e;
 }
 
+template <int M, bool C>
+static cudaError_t set_sort_scatter_limit() {
+  return cudaFuncSetAttribute(sort_scatter_kernel<M, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sort_scatter_smem(SORT_MAX_EXPERTS, SORT_SMALL_MAX_PAIRS));
+}
+
 cudaError_t prep_set_smem_limits() {
   cudaError_t e = cudaFuncSetAttribute(sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sort_small_smem(SORT_MAX_EXPERTS));
   if (e != cudaSuccess) return e;
+  if ((e = set_sort_scatter_limit<SW_A16, false>()) != cudaSuccess) return e;
+  if ((e = set_sort_scatter_limit<SW_A8, false>()) != cudaSuccess) return e;
+  if ((e = set_sort_scatter_limit<SW_A8, true>()) != cudaSuccess) return e;
+  if ((e = set_sort_scatter_limit<SW_A4, false>()) != cudaSuccess) return e;
+  if ((e = set_sort_scatter_limit<SW_A4, true>()) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(sort_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)((size_t)SORT_MAX_EXPERTS * 36));
   return e;
@@ -533,21 +671,24 @@ cudaError_t launch_act_quant(const void* x, int T, int H, int fmt, uint8_t* xq, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row, uint8_t* codes,
-                               uint8_t* scales, int scale_stride, float* acc32, const float* topk_w, int32_t* row_tok,
-                               float* row_w, int num_sms, cudaStream_t st) {
+static long scatter_blocks(int T, int H, int threads, int num_sms) {
   const long work = (long)T * (H / 32);  // 32-blocks, four threads each
-  long blocks = (work * 4 + 127) / 128;
-  const long floor_blocks = ((long)T * H / 4 + 127) / 128;  // enough threads to zero acc32 quickly
+  long blocks = (work * 4 + threads - 1) / threads;
+  const long floor_blocks = ((long)T * H / 4 + threads - 1) / threads;  // enough threads to zero acc32 quickly
   if (blocks < floor_blocks / 4) blocks = floor_blocks / 4;
-  const long cap = (long)num_sms * 16;
+  const long cap = (long)num_sms * (threads == 128 ? 16 : 1);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  return blocks;
+}
+
+cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row,
+                               const ScatterOut& so, int num_sms, cudaStream_t st) {
+  const long blocks = scatter_blocks(T, H, 128, num_sms);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  const bool chunk = scale_stride == 0;
+  const bool chunk = so.sstride == 0;
 #define MOE_SCATTER(M, C) \
-  launch_k(act_scatter_kernel<M, C>, dim3((unsigned)blocks), dim3(128), 0, st, true, xb, T, H, K, pair_row, codes, \
-           scales, scale_stride, acc32, topk_w, row_tok, row_w)
+  launch_k(act_scatter_kernel<M, C>, dim3((unsigned)blocks), dim3(128), 0, st, true, xb, T, H, K, pair_row, so)
   cudaError_t e;
   if (mode == SW_A16) e = MOE_SCATTER(SW_A16, false);
   else if (mode == SW_A8 && chunk) e = MOE_SCATTER(SW_A8, true);
@@ -555,6 +696,35 @@ cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, con
   else if (chunk) e = MOE_SCATTER(SW_A4, true);
   else e = MOE_SCATTER(SW_A4, false);
 #undef MOE_SCATTER
+  return e;
+}
+
+size_t sort_scatter_smem(int E, long n) {
+  return (size_t)E * 8 + 32 * 4 + (size_t)((n + 3) & ~3L) * 4 + (size_t)E * 32;
+}
+
+cudaError_t launch_sort_scatter(const int32_t* ids, long n, int E, int tile_m, const SortOut& so, int* err,
+                                const void* x, int T, int H, int K, int mode, const ScatterOut& sc, int num_sms,
+                                cudaStream_t st) {
+  if (n > SORT_SMALL_MAX_PAIRS) return cudaErrorInvalidValue;
+  // every CTA repeats the sort, so the scatter is spread only as far as its work
+  // needs: about 64 (token, 32-block) units per CTA, up to one CTA per SM
+  long blocks = ((long)T * (H / 32) + 63) / 64;
+  if (blocks > num_sms) blocks = num_sms;
+  if (blocks < 1) blocks = 1;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  const bool chunk = sc.sstride == 0;
+  const size_t smem = sort_scatter_smem(E, n);
+#define MOE_SORT_SCATTER(M, C)                                                                                \
+  launch_k(sort_scatter_kernel<M, C>, dim3((unsigned)blocks), dim3(1024), smem, st, true, ids, (int)n, E, tile_m, \
+           so, err, xb, T, H, K, sc)
+  cudaError_t e;
+  if (mode == SW_A16) e = MOE_SORT_SCATTER(SW_A16, false);
+  else if (mode == SW_A8 && chunk) e = MOE_SORT_SCATTER(SW_A8, true);
+  else if (mode == SW_A8) e = MOE_SORT_SCATTER(SW_A8, false);
+  else if (chunk) e = MOE_SORT_SCATTER(SW_A4, true);
+  else e = MOE_SORT_SCATTER(SW_A4, false);
+#undef MOE_SORT_SCATTER
   return e;
 }
 

@@ -17,11 +17,13 @@
 //           path..."), scale_vec::2X, K tile 256.
 //   SW_A16: bf16 activations ("Retune Kimi-K3 a16w4 MoE tile geometry"), on
 //           kind::mxf4 like SW_A4: each bf16 value is carried as the sum of
-//           kTerms = 5 e2m1 codes, each term with its own 1x32 e8m0 scale (term
+//           kTerms = 6 e2m1 codes, each term with its own 1x32 e8m0 scale (term
 //           t quantises, by the MX rule, what the earlier terms left over).
-//           The sum reproduces ~99.6% of bf16 values exactly and the rest
-//           within ~3e-6 relative (L2), far inside bf16's own rounding (~2e-3);
-//           the weights stay packed. The terms of sorted row r are stored as
+//           Each term lowers the block's scale exponent by at least 2 and leaves
+//           a residual below twice its own scale, so after n terms every value
+//           is within 2^(1-2n) of its 32-block's maximum (2^-11 for six); on
+//           N(0,1) data 99.97% of values come out exact. The weights stay
+//           packed. The terms of sorted row r are stored as
 //           sub-rows r * kTerms + t, so they sit side by side in the N dimension
 //           of one MMA (column n * kTerms + t for item row n) and the weights are
 //           read once; few rows need few columns.
@@ -59,10 +61,12 @@ constexpr int kEpiWarpsSw = 4;  // warps per epilogue warpgroup; two warpgroups 
 template <int KIND> struct SwKind;
 // kNMax: routed rows per item; kTerms: code terms per value (B rows = kTerms x rows);
 // kURing: items in flight in the shared-memory ring (each slot also holds the token
-// and top-k weight of its rows). SW_A8's five unpacked operand stages leave room
+// and top-k weight of its rows). SW_A8's 5 unpacked operand stages leave room
 // for a shorter item ring.
 template <> struct SwKind<SW_A16> {
-  static constexpr int kNMax = 16, kTerms = A16_TERMS, kURing = 32;
+  // 13 rows x 6 terms = 78 sub-rows: 80 accumulator columns, which leaves TMEM room for
+  // the scale slots of nine stage-2 operand stages
+  static constexpr int kNMax = 13, kTerms = A16_TERMS, kURing = 32;
   static constexpr bool kMxf4 = true;
 };
 template <> struct SwKind<SW_A8> {
@@ -128,7 +132,7 @@ template <int KIND, int STAGE> struct SwLayout {
   static constexpr uint32_t rows = items + kURing * sizeof(UItem);     // per slot: int tok[kNMax], float w[kNMax]
   static constexpr uint32_t row_bytes = 8 * SwKind<KIND>::kNMax;
   static constexpr uint32_t bars = rows + kURing * row_bytes;
-  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 3 * kURing + kSfRing + 1) * 8;
+  static constexpr uint32_t tmem_slot = bars + (3 * kNS + 4 + 3 * kURing + kSfRing + 1) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;  // + alignment slack
 };
 
@@ -232,8 +236,9 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   static_assert(kSfRing > kSfLag && L::total <= 232448, "shared memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* empty = full + kNS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);  // a stage's TMA copies landed
+  uint64_t* sfull = full + kNS;                                 // a stage's scale chunks landed
+  uint64_t* empty = sfull + kNS;
   uint64_t* tfull = empty + kNS;
   uint64_t* tempty = tfull + 2;
   uint64_t* ufull = tempty + 2;
@@ -258,7 +263,10 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+    // full: the TMA issuer's expect_tx arrive (and the copies' bytes); sfull: the scale
+    // warp's 32 lanes. Kept apart so that the producer can wait for its own copies in
+    // flight before the CTA exits, whatever the other warps did.
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1); mbar_init(&sfull[s], 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kEpiWarpsSw); }
     // an item is released by the TMA issuer, the scale warp, the MMA issuer and the epilogue warps
     for (int s = 0; s < kURing; ++s) {
@@ -284,9 +292,16 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
-  // everything above overlapped the previous kernel's tail; its results are read from here on
-  pdl_wait();
-  pdl_launch_dependents();
+  // Everything above overlapped the previous kernel's tail. Without early weights
+  // every thread waits for that kernel here. With them (the sort finished before the
+  // previous kernel began) the item list is read and the weight tiles of the first
+  // stages are loaded at once; only the activation rows, the activation scales and
+  // (through the scale warp's wait) the next kernel's launch wait for it.
+  const bool early = p.early_weights != 0;
+  if (!early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   if (warp == 3) {
     // ------------------------------ item scheduler ------------------------------
@@ -350,6 +365,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
         }
       }
     }
+    cp_async_wait<0>();  // this warp's row-token copies have landed before the CTA may exit
   } else if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     // At the start of each item the weight-scale rows of the next item are
@@ -385,6 +401,21 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
       uint32_t stage = 0;
       int it = 0;
       bool ok = true;
+      // activation-row loads of stages armed before the wait on the previous kernel
+      struct Deferred { int slot, kx, row, nbox; };
+      Deferred def[kNS];
+      int ndef = 0;
+      bool dep = !early;
+      auto flush_deferred = [&]() {
+        pdl_wait();
+        for (int i = 0; i < ndef; ++i) {
+          uint8_t* sb = smem + L::b + def[i].slot * L::b_bytes;
+          for (int bx = 0; bx < def[i].nbox; ++bx)
+            tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, def[i].kx, def[i].row + 16 * bx, &full[def[i].slot]);
+        }
+        ndef = 0;
+        dep = true;
+      };
       while (ok) {
         const int us = it % kURing;
         if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
@@ -398,6 +429,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
         const uint32_t btx = (uint32_t)nbox * 16 * C::kRow;
         for (int ks = 0; ks < ktiles; ++ks, ++stage) {
           const int slot = stage % kNS;
+          if (!dep && ndef == kNS) flush_deferred();  // the ring is full of weight-only stages
           if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + L::a + slot * L::a_bytes;
           uint8_t* sb = smem + L::b + slot * L::b_bytes;
@@ -412,10 +444,19 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
           }
           // routed rows: contiguous sub-rows [row0 * kTerms, (row0 + nrows) * kTerms), 16-row boxes
           // (rows past this expert belong to later experts and only fill unused columns)
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, kx, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
+          if (dep) {
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, kx, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
+          } else {
+            def[ndef++] = Deferred{slot, kx, ui.row0 * KD::kTerms, nbox};
+          }
         }
       }
+      if (!dep) flush_deferred();  // fewer stages than the ring holds (or an early end)
+      // every copy this thread started has landed before the CTA may exit (after an
+      // abort nobody else waits for them); in a normal run these return at once
+      for (uint32_t g = stage > (uint32_t)kNS ? stage - kNS : 0u; g < stage; ++g)
+        mbar_wait(&full[g % kNS], (g / kNS) & 1, p.err);
     }
   } else if (warp == 1) {
     // ---------- e8m0 scales of both operands into tcgen05.cp chunks ----------
@@ -423,6 +464,10 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
     // g - kSfRing); warp 1 arrives on the operand slot's full barrier kSfLag stages
     // later, once its copies have landed, after checking that the operand slot
     // has been re-armed for that stage.
+    if (early) {  // activation scales come from the previous kernel
+      pdl_wait();
+      pdl_launch_dependents();
+    }
     const int sb_w = kdim / 32;  // weight-scale bytes per row
     uint32_t stage = 0, pend = 0;
     int it = 0;
@@ -431,7 +476,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
       const uint32_t g = stage - pend;
       // the operand slot of stage g is in g's phase once the MMA released stage g - kNS
       ok = ok && warp_wait(&empty[g % kNS], ((g / kNS) & 1) ^ 1, p.err, &abort_flag);
-      mbar_arrive(&full[g % kNS]);
+      mbar_arrive(&sfull[g % kNS]);
       --pend;
     };
     while (ok) {
@@ -516,7 +561,11 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
         const uint32_t dg = tbase + buf * 2 * kAccCols;
         bool ok = true;
         for (int ks = 0; ks < ktiles; ++ks) {
-          if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag)) { ok = false; break; }
+          if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag) ||
+              !mbar_wait_or_abort(&sfull[slot], phase, p.err, &abort_flag)) {
+            ok = false;
+            break;
+          }
           tc::fence_after();
           constexpr uint32_t kOpCols = 4 * C::kChunks;  // TMEM columns of one operand's scale chunks
           const uint32_t sfc = sf0 + slot * C::kSfCols;  // sfa tile 0, sfa tile 1, sfb: kOpCols apart
@@ -668,6 +717,31 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
               float* dst = p.acc32 + (size_t)t * H + h0;
               atomicAdd(dst, w * v0[n]);
               if (h1ok) atomicAdd(dst + 128, w * v1[n]);
+            }
+          }
+          if (p.tok_cnt) {
+            // Finalize folded in: each row counts its arrival on its token's counter for
+            // this (slice, quadrant); the warp that brings a counter to zero holds the last
+            // contribution and writes those 32 + 32 values of out as bf16 (RNE).
+            __threadfence();  // this warp's adds are performed before they are counted
+            const int col = c0 + lane;
+            const int ta = __shfl_sync(0xFFFFFFFFu, tok_a, col & 31);
+            const int tb = __shfl_sync(0xFFFFFFFFu, tok_b, col & 31);
+            const int tl = col < 32 ? ta : tb;
+            bool last = false;
+            if (lane < nn) last = atomicSub(p.tok_cnt + ((size_t)tl * p.nsl + ui.tile) * 4 + q, 1) == 1;
+            unsigned done = __ballot_sync(0xFFFFFFFFu, last);
+            if (done) {
+              __threadfence();  // the other contributors' adds are visible from here on
+              while (done) {
+                const int n = __ffs(done) - 1;
+                done &= done - 1;
+                const int t = __shfl_sync(0xFFFFFFFFu, tl, n);
+                const float* src = p.acc32 + (size_t)t * H + h0;
+                __nv_bfloat16* o = p.out + (size_t)t * H + h0;
+                o[0] = __float2bfloat16_rn(__ldcg(src));
+                if (h1ok) o[128] = __float2bfloat16_rn(__ldcg(src + 128));
+              }
             }
           }
         }

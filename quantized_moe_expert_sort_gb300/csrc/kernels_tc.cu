@@ -17,6 +17,13 @@
 // and requantises y per 32 along I by itself. Stage 2: N = 128 rows of H; each
 // thread adds w * z for its row into the fp32 combine buffer (vector red).
 //
+// Tile order: stage 1 runs block-major (the N tiles of one 128-row block back to
+// back, so the block's activations are re-read from L2). Stage 2 adds into the
+// fp32 combine buffer; when that buffer is larger than L2 the N tiles are taken
+// in groups of p.tile_group (block-major inside a group), so the CTAs in flight
+// add into a slice of T x 128 x tile_group fp32 that stays in L2 instead of
+// into random rows of the whole buffer.
+//
 // CTA (one per SM, persistent over tiles): warp 0 issues all loads with TMA /
 // bulk copies -- the 128 sorted rows (stage 1 reads activations the quantiser
 // wrote in sorted order, stage 2 the intermediate), the weight tile, the rows'
@@ -60,6 +67,17 @@ template <> struct Kind<TC_A4W4> {
 // they are, so the B tiles are zeroed once at kernel start).
 template <int KIND> constexpr uint32_t weight_tile_tx() { return KIND == TC_A8W4 ? kTileBytes / 2 : kTileBytes; }
 
+// (block, N tile) of a linear tile index: N tiles in groups of G (the last group
+// may be smaller), block-major inside a group. G >= ntn is plain block-major.
+__device__ __forceinline__ void tile_coords(int tile, int nb, int ntn, int G, int* b, int* nt) {
+  const int gsz = nb * G;
+  const int g = tile / gsz;
+  const int r = tile - g * gsz;
+  const int gg = min(G, ntn - g * G);
+  *b = r / gg;
+  *nt = g * G + r % gg;
+}
+
 struct TcLayout {
   static constexpr uint32_t a = 0;                                  // kNS x 16 KB
   static constexpr uint32_t b = a + kNS * kTileBytes;               // kNS x 16 KB
@@ -70,7 +88,7 @@ struct TcLayout {
   static constexpr uint32_t epi = ws + 2 * ws_bytes;               // stage-2 transpose: per epilogue warp 32 x 36 fp32
   static constexpr uint32_t epi_bytes = 32 * 36 * 4;
   static constexpr uint32_t bars = epi + kEpiWarps * epi_bytes;
-  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 8) * 8;
+  static constexpr uint32_t tmem_slot = bars + (3 * kNS + 8) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;        // + alignment slack
 };
 
@@ -102,8 +120,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   using KD = Kind<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);
-  uint64_t* empty = full + kNS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);  // a stage's TMA copies landed
+  uint64_t* sfull = full + kNS;                                        // a stage's weight scales transposed
+  uint64_t* empty = sfull + kNS;
   uint64_t* tfull = empty + kNS;
   uint64_t* tempty = tfull + 2;
   uint64_t* wsfull = tempty + 2;   // weight scales of a tile landed in staging
@@ -123,12 +142,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   const int ktiles = (kdim + KD::kKTile - 1) / KD::kKTile;
   const int nblk_k = kdim / 32;                       // valid 32-blocks along K
   const int ntn = STAGE == 1 ? I / 64 : H / kBN;      // N tiles per expert
-  const int num_tiles = p.meta[META_NUM_BLOCKS] * ntn;
+  const int G = STAGE == 1 || p.tile_group <= 0 ? ntn : p.tile_group;  // N tiles per group (tile order)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // full: the TMA issuer's expect_tx arrive + the 32 scale-copy lanes
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
+    // full: the TMA issuer's expect_tx arrive (and the copies' bytes); sfull: the 32
+    // scale-transpose lanes. Kept apart so that a producer can wait for its own
+    // copies in flight, whatever the other warps did.
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1); mbar_init(&sfull[s], 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], kEpiWarps);
@@ -155,6 +176,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   // everything above overlapped the previous kernel's tail; its results are read from here on
   pdl_wait();
   pdl_launch_dependents();
+  const int nb = p.meta[META_NUM_BLOCKS];
+  const int num_tiles = nb * ntn;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -164,8 +187,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
       const int sb_row = kdim / 32;  // weight-scale bytes per row
       uint32_t stage = 0;
       int lt = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-        const int b = tile / ntn, nt = tile % ntn;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
+        int b, nt;
+        tile_coords(tile, nb, ntn, G, &b, &nt);
         const int e = p.block_expert[b];
         // the tile's weight scales, row-major, into the staging buffer of this tile parity
         const int tp = lt & 1;
@@ -181,7 +206,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         }
         for (int ks = 0; ks < ktiles; ++ks, ++stage) {
           const int slot = stage % kNS;
-          if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
+          if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + TcLayout::a + slot * kTileBytes;
           uint8_t* sb = smem + TcLayout::b + slot * kTileBytes;
           int nchunk = 0;  // row-scale chunks of this stage inside K (the rest are filled by the scale warp)
@@ -201,19 +226,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
                      p.as + ((size_t)b * (nblk_k / 4) + (ks * KD::kBlocks) / 4 + c) * 512, 512u, &full[slot]);
         }
       }
+      // Before the CTA may exit, every copy this thread started must have landed
+      // (after an abort the consumers no longer wait for them): the last kNS
+      // operand stages and the last two scale stagings. In a normal run these
+      // phases completed long ago and the waits return at once.
+      for (uint32_t g = stage > (uint32_t)kNS ? stage - kNS : 0u; g < stage; ++g)
+        mbar_wait(&full[g % kNS], (g / kNS) & 1, p.err);
+      for (int l = lt > 2 ? lt - 2 : 0; l < lt; ++l) mbar_wait(&wsfull[l & 1], (l >> 1) & 1, p.err);
     }
   } else if (warp == 1) {
     // ---------------- weight scales: staging (row-major) -> tcgen05.cp chunks ----------------
     const int sb_row = kdim / 32;
     uint32_t stage = 0;
     int lt = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
       const int tp = lt & 1;
       if (!mbar_wait_or_abort(&wsfull[tp], (lt >> 1) & 1, p.err, &abort_flag)) break;
       const uint8_t* wst = smem + TcLayout::ws + tp * TcLayout::ws_bytes;
       for (int ks = 0; ks < ktiles; ++ks, ++stage) {
         const int slot = stage % kNS;
-        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) break;
+        if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
         uint8_t* dA = smem + TcLayout::sfa + slot * 1024;
         uint8_t* dB = smem + TcLayout::sfb + slot * 1024;
         for (int c = 0; c < KD::kChunks; ++c) {
@@ -230,9 +263,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           }
         }
         fence_proxy_async();  // generic smem writes -> visible to tcgen05.cp
-        mbar_arrive(&full[slot]);
+        mbar_arrive(&sfull[slot]);
       }
       __syncwarp();
+      if (!ok) break;
       mbar_arrive(&wsempty[tp]);
     }
   } else if (warp == 2) {
@@ -248,14 +282,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
                                                : tc::idesc_bs(kBM, kBN, tc::MXF4_E2M1, tc::MXF4_E2M1, 0, 0);
       uint32_t stage = 0;
       int lt = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++lt) {
         const int buf = lt & 1;
-        mbar_wait_or_abort(&tempty[buf], ((lt >> 1) & 1) ^ 1, p.err, &abort_flag);
+        if (!mbar_wait_or_abort(&tempty[buf], ((lt >> 1) & 1) ^ 1, p.err, &abort_flag)) break;
         tc::fence_after();
         const uint32_t d = tbase + buf * kBN;
         for (int ks = 0; ks < ktiles; ++ks, ++stage) {
           const int slot = stage % kNS;
-          mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag);
+          // an aborted wait leaves the stage unread: no MMA runs on operands that never landed
+          if (!mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag) ||
+              !mbar_wait_or_abort(&sfull[slot], (stage / kNS) & 1, p.err, &abort_flag)) {
+            ok = false;
+            break;
+          }
           tc::fence_after();
           const uint32_t sfa = tbase + kSfCol0 + slot * 16;
           const uint32_t sfb = sfa + 8;
@@ -278,6 +318,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           }
           tc::commit(&empty[slot]);
         }
+        if (!ok) break;  // a partial accumulator is never handed to the epilogue
         tc::commit(&tfull[buf]);
       }
       // every MMA / copy this thread issued has finished before TMEM is released
@@ -292,13 +333,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
-      const int b = tile / ntn, nt = tile % ntn;
+      int b, nt;
+      tile_coords(tile, nb, ntn, G, &b, &nt);
       const int buf = lt & 1;
       const int row = b * kBM + m;
       const int pid = p.sorted_ids[row];
       const bool valid = pid < TK;
-      mbar_wait_or_abort(&tfull[buf], (lt >> 1) & 1, p.err, &abort_flag);
+      // a timed-out wait means the accumulator never completed: no store or reduction
+      bool ready = true;
+      if (lane == 0) ready = mbar_wait_or_abort(&tfull[buf], (lt >> 1) & 1, p.err, &abort_flag);
+      ready = __shfl_sync(0xFFFFFFFFu, ready ? 1 : 0, 0) != 0;
       __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp, converged
+      if (!ready) break;
       tc::fence_after();
       const uint32_t d = tbase + lane_off + buf * kBN;
       if (STAGE == 1) {

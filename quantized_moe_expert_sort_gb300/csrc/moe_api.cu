@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -58,6 +59,10 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Host-side fault injection (moe_debug_inject): the index of the workspace
+// allocation the next moe_create fails, or -1. One-shot.
+std::atomic<long> g_fail_alloc{-1};
+
 }  // namespace
 
 void moe::set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
@@ -86,6 +91,12 @@ struct moe_ctx {
   const void* tm_w2sw_key; CUtensorMap tm_w2sw;  // packed w2, 64-byte rows (few-rows stage 2)
   int last_inter_stride;
   int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
+  int tc_group;     // many-rows stage 2: N tiles per group of the tile order (0: chosen per call)
+  int fused;        // 1: sort + scatter in one launch (calls of up to SORT_SMALL_MAX_PAIRS pairs)
+  int fold;         // 1: the few-rows stage 2 writes out itself (no finalize launch)
+  int early;        // 1: the few-rows stages load weights before waiting on their predecessor
+  int nsl;          // 256-row slices of H (stage-2 arrival counters)
+  int* tok_cnt;     // [max_tokens][nsl][4] stage-2 arrival counters
   int last_inter_layout;
   int last_tile_m;
   // profiling (moe_set_profiling)
@@ -106,7 +117,7 @@ static void free_ctx(moe_ctx* c) {
   void* ptrs[] = {c->sorted_ids, c->block_expert, c->expert_count, c->expert_offset, c->active_experts,
                   c->meta, c->hist, c->xq, c->xs, c->inter_q, c->inter_s, c->acc32, c->err,
                   c->xq_sorted, c->xs_sorted, c->pair_row, c->row_tok, c->row_w, c->active_info,
-                  c->st_x, c->st_ids, c->st_w, c->st_out};
+                  c->st_x, c->st_ids, c->st_w, c->st_out, c->tok_cnt};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (cudaEvent_t e : c->ev)
@@ -271,6 +282,7 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   c->cap_blocks = c->cap_rows;  // enough for tile_m = 1
   c->hist_chunks = (int)((pairs + SORT_CHUNK - 1) / SORT_CHUNK);
   if (c->hist_chunks < 1) c->hist_chunks = 1;
+  c->nsl = (H + 255) / 256;
 
   struct { void** p; size_t bytes; } allocs[] = {
       {(void**)&c->sorted_ids, sizeof(int32_t) * c->cap_rows},
@@ -296,14 +308,19 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->st_ids, sizeof(int32_t) * pairs},
       {(void**)&c->st_w, sizeof(float) * pairs},
       {(void**)&c->st_out, (size_t)max_tokens * H * 2},
+      {(void**)&c->tok_cnt, sizeof(int) * (size_t)max_tokens * c->nsl * 4},
   };
+  const long inject = g_fail_alloc.exchange(-1);
+  long idx = 0;
   for (auto& a : allocs) {
-    cudaError_t e = cudaMalloc(a.p, a.bytes);
+    cudaError_t e = idx == inject ? cudaErrorMemoryAllocation : cudaMalloc(a.p, a.bytes);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      free_ctx(c);
-      return fail(MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", a.bytes, cudaGetErrorString(e));
+      free_ctx(c);  // releases every buffer allocated so far
+      return fail(MOE_ERR_OOM, "cudaMalloc(%zu) failed%s: %s", a.bytes, idx == inject ? " (injected)" : "",
+                  cudaGetErrorString(e));
     }
+    ++idx;
   }
   cudaError_t e = cudaMemset(c->err, 0, sizeof(int) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->meta, 0, sizeof(int32_t) * META_WORDS);
@@ -316,6 +333,13 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   }
   c->tc_min_rows = 32;
   if (const char* v = getenv("MOE_TC_MIN_ROWS")) c->tc_min_rows = atoi(v);
+  if (const char* v = getenv("MOE_TC_GROUP")) c->tc_group = atoi(v);
+  c->fused = 0;
+  if (const char* v = getenv("MOE_FUSED")) c->fused = atoi(v);
+  c->fold = 0;
+  if (const char* v = getenv("MOE_FOLD")) c->fold = atoi(v);
+  c->early = 1;
+  if (const char* v = getenv("MOE_EARLY")) c->early = atoi(v);
   c->last_inter_stride = scale_row_stride(I);
   *out = c;
   return MOE_OK;
@@ -340,6 +364,10 @@ moe_status moe_get_workspace(moe_ctx* c, moe_workspace_view* v) {
   v->act_scale_stride = scale_row_stride(c->H);
   v->inter_scale_stride = c->last_inter_stride;
   v->inter_scale_layout = c->last_inter_layout;
+  v->act_sorted_codes = c->xq_sorted;
+  v->act_sorted_scales = c->xs_sorted;
+  v->act_sorted_scale_stride = scale_row_stride(c->H);
+  v->a16_terms = A16_TERMS;
   return MOE_OK;
 }
 
@@ -432,23 +460,44 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   }
 
   c->ev_n = 0;
-  prof_mark(c, st, "sort");
   SortOut so = sort_out(c);
   so.pair_row = c->pair_row;
   if (use_sw) so.active_info = c->active_info;
-  cudaError_t e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
-  if (e != cudaSuccess) return cuda_fail(e, "sort launch");
   c->last_tile_m = tile_m;
   c->last_inter_layout = use_tc ? 1 : (adt == MOE_A_BF16 ? 2 : 0);
   c->last_inter_stride = use_sw ? is_sw : scale_row_stride(c->I);
-  prof_mark(c, st, "act_quant");
-  if (use_tc)
-    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, 0, c->acc32, nullptr,
-                           nullptr, nullptr, c->num_sms, st);
-  else
-    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, c->xq_sorted, c->xs_sorted, xs_sw, c->acc32, w,
-                           c->row_tok, c->row_w, c->num_sms, st);
-  if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+  // the few-rows stage 2 writes out itself (arrival counters); the many-rows one
+  // leaves the fp32 sum for the finalize kernel
+  const bool fold = use_sw && c->fold;
+  ScatterOut sc{};
+  sc.codes = c->xq_sorted;
+  sc.scales = c->xs_sorted;
+  sc.sstride = use_tc ? 0 : xs_sw;
+  sc.acc32 = c->acc32;
+  if (use_sw) {
+    sc.topk_w = w;
+    sc.row_tok = c->row_tok;
+    sc.row_w = c->row_w;
+  }
+  if (fold) {
+    sc.tok_cnt = c->tok_cnt;
+    sc.nsl = c->nsl;
+    sc.out = static_cast<__nv_bfloat16*>(out);
+  }
+  cudaError_t e;
+  const bool one_launch = c->fused && pairs <= SORT_SMALL_MAX_PAIRS;  // sort + scatter fused
+  if (one_launch) {
+    prof_mark(c, st, "sort+act_quant");
+    e = launch_sort_scatter(ids, pairs, c->E, tile_m, so, c->err, x, T, c->H, c->K, swkind, sc, c->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sort + activation scatter launch");
+  } else {
+    prof_mark(c, st, "sort");
+    e = launch_sort(ids, pairs, c->E, tile_m, so, c->hist, c->hist_chunks, c->err, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sort launch");
+    prof_mark(c, st, "act_quant");
+    e = launch_act_scatter(x, T, c->H, c->K, swkind, c->pair_row, sc, c->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+  }
 
   StageParams p{};
   p.sorted_ids = c->sorted_ids;
@@ -475,6 +524,13 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
 
   if (use_tc) {
     long t1 = max_blocks * (c->I / 64), t2 = max_blocks * (c->H / 128);
+    // Stage-2 tile order: block-major while the fp32 combine buffer fits in L2 with
+    // room to spare; beyond that, N tiles in groups whose slice of the buffer
+    // (T x 128 columns x 4 bytes per N tile) stays near 48 MB.
+    const double acc_bytes = (double)T * c->H * 4.0, slice = (double)T * 128 * 4.0;
+    p2.tile_group = acc_bytes <= 64.0 * (1 << 20) ? 0 : (int)(48.0 * (1 << 20) / slice);
+    if (acc_bytes > 64.0 * (1 << 20) && p2.tile_group < 1) p2.tile_group = 1;
+    if (c->tc_group > 0) p2.tile_group = c->tc_group;
     prof_mark(c, st, "stage1");
     StageParams q1 = p1;
     q1.aq = c->xq_sorted;
@@ -491,6 +547,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q1.as = c->xs_sorted;
     q1.xs_stride = xs_sw;
     q1.os_stride = is_sw;
+    q1.early_weights = c->early && !one_launch;  // the sort is two kernels back
     prof_mark(c, st, "stage1");
     const long u1 = max_active * (c->I / 128);
     e = launch_swap_stage(swkind, 1, q1, c->tm_w13sw, tm_xs, (int)(u1 < c->num_sms ? u1 : c->num_sms), st);
@@ -499,15 +556,23 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q2.xs_stride = is_sw;
     q2.row_tok = c->row_tok;
     q2.row_w = c->row_w;
+    q2.early_weights = c->early;  // the sort and the scatter are at least two kernels back
+    if (fold) {
+      q2.tok_cnt = c->tok_cnt;
+      q2.nsl = c->nsl;
+      q2.out = static_cast<__nv_bfloat16*>(out);
+    }
     prof_mark(c, st, "stage2");
     e = launch_swap_stage(swkind, 2, q2, swap_row_bytes(swkind, 2) == 64 ? c->tm_w2sw : c->tm_w2tc, tm_inter,
                           (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
 
-  prof_mark(c, st, "finalize");
-  e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
-  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  if (!fold) {
+    prof_mark(c, st, "finalize");
+    e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  }
   prof_mark(c, st, "end");
   return MOE_OK;
 }
@@ -548,6 +613,24 @@ moe_status moe_quantize_activations(const void* x, int T, int H, int adt, uint8_
   return MOE_OK;
 }
 
+moe_status moe_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, void* stream) {
+  if (T < 0 || E <= 0 || E > ROUTE_MAX_EXPERTS || K <= 0 || K > E || K > ROUTE_MAX_TOPK)
+    return fail(MOE_ERR_INVALID_ARG, "bad sizes T=%d E=%d K=%d (1 <= K <= min(E, %d), E <= %d)", T, E, K,
+                ROUTE_MAX_TOPK, ROUTE_MAX_EXPERTS);
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !weights) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  static std::once_flag once[64];
+  cudaError_t se = cudaSuccess;
+  if (dev >= 0 && dev < 64) std::call_once(once[dev], [&] { se = route_set_smem_limits(); });
+  if (se != cudaSuccess) return cuda_fail(se, "router kernel attributes");
+  cudaError_t e = launch_route(logits, T, E, K, ids, weights, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  return MOE_OK;
+}
+
 moe_status moe_quantize_mxfp4(const float* w, int64_t rows, int cols, uint8_t* codes, uint8_t* scales, void* stream) {
   if (rows < 0 || cols <= 0 || cols % 32) return fail(MOE_ERR_INVALID_ARG, "bad sizes rows=%lld cols=%d", (long long)rows, cols);
   if (rows == 0) return MOE_OK;
@@ -582,6 +665,21 @@ moe_status moe_read_profile(moe_ctx* c, float* ms, const char** names, int* coun
     if (names) names[i] = c->ev_name[i];
   }
   *count = n;
+  return MOE_OK;
+}
+
+moe_status moe_debug_inject(int what, int64_t arg) {
+  if (what != MOE_INJECT_ALLOC_FAIL) return fail(MOE_ERR_INVALID_ARG, "unknown injection %d", what);
+  g_fail_alloc.store(arg < 0 ? -1 : (long)arg);
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait(moe_ctx* c, int64_t limit_ns, int complete, void* stream) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (limit_ns < 0 || limit_ns > 10000000000LL) return fail(MOE_ERR_INVALID_ARG, "limit_ns outside [0, 1e10]");
+  CUDA_TRY(cudaSetDevice(c->device));
+  cudaError_t e = launch_wait_selftest((uint64_t)limit_ns, complete, c->err, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
   return MOE_OK;
 }
 

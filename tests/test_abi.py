@@ -65,3 +65,11 @@ def test_no_gpu_means_a_clean_error():
     assert st in (1, 3)  # device out of range / CUDA error, never a crash
     with pytest.raises(moe.MoEError):
         moe.MoE(256, 128, 8, 2, 16)
+
+
+def test_fault_injection_hook_on_the_host():
+    L = moe.lib()
+    assert L.moe_debug_inject(99, 0) == 1           # unknown injection
+    assert L.moe_debug_inject(moe.INJECT_ALLOC_FAIL, 3) == 0
+    assert L.moe_debug_inject(moe.INJECT_ALLOC_FAIL, -1) == 0  # disarm
+    assert L.moe_selftest_wait(None, 1000, 0, None) == 1      # NULL context

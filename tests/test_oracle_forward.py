@@ -184,6 +184,18 @@ def test_activation_row_is_the_block_roundtrip_along_h(adt):
     assert np.array_equal(oracle.activation_row(c["x"][0], "bf16"), c["xf"][0])
 
 
+@pytest.mark.parametrize("adt", ADTS)
+def test_expert_stage1_equals_the_forward_intermediate(adt):
+    c = make_case(T=12, E=4, K=2, routing="uniform", seed=8)
+    _, _, inter, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
+                                        "situv2", 4.0, 25.0, adt, want_inter=True)
+    for e in range(4):
+        rows = np.argwhere(c["ids"] == e)  # (t, k) pairs routed to e
+        y32, yq = oracle.expert_stage1(c["x"], rows[:, 0], c["w13"][e], c["w13s"][e], "situv2", 4.0, 25.0, adt)
+        assert np.array_equal(yq, inter[rows[:, 0] * 2 + rows[:, 1]])
+        assert np.array_equal(oracle.requantize_intermediate(y32[0], adt), yq[0])
+
+
 def test_tile_m_and_subset_invariance():
     c = make_case(T=24, E=8, K=3, routing="uniform", seed=5)
     base, b16, binter, _ = oracle.moe_forward(c["x"], c["ids"], c["w"], c["w13"], c["w13s"], c["w2"], c["w2s"],
