@@ -249,6 +249,8 @@ def run_ours(args, world, rank, local, pg):
     t_setup = time.time()
     w13, w13s, w2, w2s = device_weights(device)
     ctx = moe.MoE(H, I, E, K, max(SWEEP_T + [args.tokens]) if not args.no_sweep else args.tokens, device=local)
+    if args.prepack:  # load-time repack of the stage-2 weights (few-rows path)
+        ctx.prepack(w2, w2s, CFG.a_dtype)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     clean_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -403,6 +405,7 @@ def run_ours(args, world, rank, local, pg):
                    "l2": "flushed before every timed step (256 MB memset, then a 256 MB read so that no dirty "
                          "line is written back inside the step; both outside the events)",
                    "active_experts": n_active, "routed_pairs": n_pairs,
+                   "w2_prepacked": bool(args.prepack),
                    "sweep_us_per_call": sweep, "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor" if tensor_bound else "hbm", "kernel": dominant,
                      "achieved": round(achieved, 1), "peak": round(kpeak, 1), "peak_source": ksrc, "unit": kunit,
@@ -422,7 +425,53 @@ def run_ours(args, world, rank, local, pg):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.tokens, args.cpu_sample)
+    if args.prefill and args.config == "tp8_decode":
+        del ctx, w13, w13s, w2, w2s
+        torch.cuda.empty_cache()
+        result["prefill"] = prefill_table(device, flush, pg, world)
+        select_config(args.config)
     return result
+
+
+PREFILL_ROWS = [("tp8_a8", 4096, "situv2"), ("ep_wide", 8192, "situv2"), ("tp8_a4_zipf", 32768, "situv2")]
+
+
+def prefill_table(device, flush, pg, world, steps=5, warmup=3):
+    """The prefill workloads: us/call, governing bound and call fraction of the
+    roofline (whole call; the slower of its bytes at HBM and its FLOPs at the
+    tensor peak of its MMA kind), L2 flushed before every timed call."""
+    import quantized_moe_expert_sort_gb300 as moe
+    rows = {}
+    for name, T, act in PREFILL_ROWS:
+        select_config(name)
+        w13, w13s, w2, w2s = device_weights(device)
+        ctx = moe.MoE(H, I, E, K, T, device=device.index or 0)
+        x, ids, w, xd, idd, wd = batch(T, device)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        ms = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            ctx.forward(xd, idd, wd, w13, w13s, w2, w2s, act, 4.0, 25.0, CFG.a_dtype, out=out)
+            e.record()
+            torch.cuda.synchronize(device)
+            if i >= warmup:
+                ms.append(s.elapsed_time(e))
+        us = max_over_ranks(pg, statistics.mean(ms), device) * 1000.0 / world
+        srt = ctx.last_sort()
+        n_pairs = int((srt["sorted_ids"] < T * K).sum().item())
+        ab = algo_bytes(T, srt["num_active"], n_pairs)
+        peak, _ = measured_peaks()
+        tpeak, _ = tensor_peak_tflops(CFG.a_dtype)
+        t_bytes, t_flops = ab["call"] / (peak * 1e9), 6.0 * n_pairs * H * I / (tpeak * 1e12)
+        rows["%s_T%d" % (name, T)] = {"us_per_call": round(us, 1), "bound": "tensor" if t_flops > t_bytes else "hbm",
+                                      "call_frac": round(max(t_bytes, t_flops) / (us * 1e-6), 4),
+                                      "a_dtype": CFG.a_dtype, "act": act, "path_tile_m": srt["tile_m"]}
+        log("prefill %s T=%d: %.1f us" % (name, T, us))
+        del ctx, w13, w13s, w2, w2s, out
+        torch.cuda.empty_cache()
+    return rows
 
 
 # ---------------------------------------------------------------------------
@@ -502,6 +551,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16)
     ap.add_argument("--ref-sample", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prepack", action="store_true", help="stage 2 reads a prepacked copy of w2 (moe_prepack)")
+    ap.add_argument("--prefill", type=int, default=1, help="add the prefill table (default workload only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -262,6 +262,25 @@ moe_status moe_set_profiling(moe_ctx* ctx, int enable);
  * *count is the capacity on entry and the number written on return. */
 moe_status moe_read_profile(moe_ctx* ctx, float* ms, const char** names, int* count);
 
+/* Prepacked stage-2 weights (an optimisation of the few-rows path; the plain
+ * layout stays the contract and is still needed by the many-rows path).
+ * moe_prepack_size: bytes of the packed copy (as many as w2 + w2_scale).
+ * moe_prepack: enqueues on `stream` a copy of w2 [E,H,I/2] / w2_scale [E,H,I/32]
+ * (device) into `packed` (device, caller-owned, 16-byte aligned, size above) as
+ * contiguous blocks, one per (expert e, 128-row tile ht of H, 128-element chunk kc
+ * of I): codes, 8 KB per block, row r (0..127) at block byte 64 r, holding
+ * w2[e, 128 ht + r, 64 kc .. 64 kc + 63] -- for a_dtype bf16 and fp4 with the
+ * 16-byte chunk c of row r stored at chunk c ^ ((r / 2) % 4) (the image the
+ * kind::mxf4 kernels read), for fp8 in order; then the scales, 512 bytes per
+ * block, byte 16*(r%32) + 4*(r/32) + b = w2_scale[e, 128 ht + r, 4 kc + b].
+ * It binds the copy to ctx: later moe_forward calls with this same w2 pointer
+ * and this a_dtype read it on the few-rows path. The caller keeps `packed`
+ * alive and unchanged while bound; packed == NULL unbinds. Redo it if w2
+ * changes. */
+moe_status moe_prepack_size(moe_ctx* ctx, int64_t* bytes);
+moe_status moe_prepack(moe_ctx* ctx, const uint8_t* w2, const uint8_t* w2_scale, int a_dtype, void* packed,
+                       void* stream);
+
 /* Failure-detection support (no GPU fault is involved in either).
  * moe_selftest_wait: one warp waits on a shared-memory barrier with the same
  * bounded wait every pipeline stage uses, but with a limit of limit_ns

@@ -66,6 +66,8 @@ def lib():
         L.moe_quantize_mxfp4.argtypes = [vp, i64, i32, vp, vp, vp]
         L.moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_selftest_wait.argtypes = [vp, i64, i32, vp]
+        L.moe_prepack_size.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
+        L.moe_prepack.argtypes = [vp, vp, vp, i32, vp, vp]
         L.moe_debug_inject.argtypes = [i32, i64]
         L.moe_get_workspace.argtypes = [vp, ctypes.POINTER(_WorkspaceView)]
         L.moe_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -78,7 +80,7 @@ def lib():
         L.moe_last_error_message.argtypes = []
         for name in ("moe_create", "moe_destroy", "moe_sort", "moe_forward", "moe_forward_host",
                      "moe_quantize_activations", "moe_quantize_mxfp4", "moe_route", "moe_get_workspace",
-                     "moe_selftest_wait", "moe_debug_inject", "moe_get_error",
+                     "moe_selftest_wait", "moe_debug_inject", "moe_prepack_size", "moe_prepack", "moe_get_error",
                      "moe_set_profiling", "moe_read_profile"):
             getattr(L, name).restype = i32
         _lib = L
@@ -253,6 +255,23 @@ class MoE:
         n = ctypes.c_int(8)
         _check(lib().moe_read_profile(self._h, ms, names, ctypes.byref(n)))
         return [(names[i].decode(), float(ms[i])) for i in range(n.value)]
+
+    def prepack(self, w2, w2_scale, a_dtype="bf16", stream=None):
+        """Copy w2 / w2_scale into the few-rows stage-2 block layout for a_dtype and bind the
+        copy to this context (used by forward calls with this same w2 and a_dtype). Returns
+        the packed tensor, which must be kept alive while bound."""
+        _require(w2, torch.uint8, "w2")
+        _require(w2_scale, torch.uint8, "w2_scale")
+        n = ctypes.c_int64(0)
+        _check(lib().moe_prepack_size(self._h, ctypes.byref(n)))
+        packed = torch.empty(n.value, dtype=torch.uint8, device=w2.device)
+        _check(lib().moe_prepack(self._h, _ptr(w2), _ptr(w2_scale), ADTYPE[a_dtype], _ptr(packed), _stream(stream)))
+        self._packed = packed
+        return packed
+
+    def unbind_prepacked(self):
+        _check(lib().moe_prepack(self._h, None, None, 0, None, None))
+        self._packed = None
 
     def selftest_wait(self, limit_ns, complete, stream=None):
         """Run the bounded-wait self-test kernel (see moe_selftest_wait)."""

@@ -94,10 +94,14 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
 // ---------------------------------------------------------------------------
 // Activation functions (aiter PR 6259 Motivation, PR 4471 Motivation)
 // sigmoid(z) = 1 / (1 + 2^(-z * log2 e)) with the hardware exp2 and reciprocal
-// (no cancellation: a few ulp). tanh is CUDA's tanhf: the int4 SiTUv2 page
-// builds tanh as 2 * sigmoid(2z) - 1, which in fp32 cancels for small z (up to
-// ~4e-4 relative at the |u| / linear_beta of small activations); tanhf keeps the
-// relative error at a few ulp and still saturates to exactly +-1 for large |z|.
+// (no cancellation: a few ulp).
+// tanh: the int4 SiTUv2 page builds it as 2 * sigmoid(2z) - 1, which saturates to
+// +-1 at both ends; in fp32 that difference cancels for small z (the sigmoid's
+// ~1e-7 absolute error becomes ~4e-4 relative at the |u| / linear_beta of small
+// activations). For |z| < 1/4 the odd Taylor series of tanh,
+//   z - z^3/3 + 2 z^5/15 - 17 z^7/315 + 62 z^9/2835,
+// is used instead (truncation below 2e-8 relative there); above 1/4 the
+// cancellation costs at most ~2e-6 relative.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float fast_sigmoid(float z) {
   float e, r;
@@ -106,12 +110,30 @@ __device__ __forceinline__ float fast_sigmoid(float z) {
   return r;
 }
 
+__device__ __forceinline__ float tanh_act(float z) {
+  if (fabsf(z) < 0.25f) {
+    const float z2 = z * z;
+    float p = 62.0f / 2835.0f;
+    p = fmaf(p, z2, -17.0f / 315.0f);
+    p = fmaf(p, z2, 2.0f / 15.0f);
+    p = fmaf(p, z2, -1.0f / 3.0f);
+    return fmaf(z * z2, p, z);
+  }
+  return 2.0f * fast_sigmoid(2.0f * z) - 1.0f;
+}
+
+// kAccurate: tanh_act (the bf16 intermediate of the a16 path keeps 8 bits of every
+// value); otherwise 2 * sigmoid(2z) - 1 throughout, whose worst relative error
+// (~4e-4 at small z) lies far inside the fp8 / fp4 steps the intermediate is
+// requantised to.
+template <bool kAccurate = true>
 __device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta) {
   const float sig = fast_sigmoid(g);
   if (act == ACT_SILU) return g * sig * u;
-  const float situ = beta * tanhf(g / beta) * sig;
-  const float up = lbeta * tanhf(u / lbeta);
-  return situ * up;
+  if (kAccurate) return beta * tanh_act(g / beta) * sig * (lbeta * tanh_act(u / lbeta));
+  const float tg = 2.0f * fast_sigmoid(2.0f * g / beta) - 1.0f;
+  const float tu = 2.0f * fast_sigmoid(2.0f * u / lbeta) - 1.0f;
+  return beta * tg * sig * (lbeta * tu);
 }
 
 // ---------------------------------------------------------------------------

@@ -77,9 +77,6 @@ struct ScatterOut {
   const float* topk_w;  // row_tok / row_w (optional): token and top-k weight of every sorted row
   int32_t* row_tok;
   float* row_w;
-  int* tok_cnt;         // stage-2 arrival counters [T][nsl][4] (finalize inside stage 2), or nullptr;
-  int nsl;              // set to the token's number of routed pairs; nsl = 256-row slices of H
-  __nv_bfloat16* out;   // with tok_cnt: rows of tokens without a routed pair are zeroed here
 };
 cudaError_t launch_act_scatter(const void* x, int T, int H, int K, int mode, const int32_t* pair_row,
                                const ScatterOut& so, int num_sms, cudaStream_t st);
@@ -92,6 +89,13 @@ cudaError_t launch_sort_scatter(const int32_t* ids, long n, int E, int tile_m, c
 // One warp waits on an mbarrier with a limit of limit_ns (complete != 0: the
 // barrier completes first); a wait that runs out sets DEV_ERR_TIMEOUT in *err.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int complete, int* err, cudaStream_t st);
+
+// Stage-2 weights repacked for the few-rows kernels (kernels_pack.cu): codes as 8 KB
+// blocks [E][H/128][I/128][128 rows][64 bytes] (swz: each block pre-swizzled as the
+// 64-byte-swizzle shared-memory image), scales as 512-byte tcgen05.cp chunks
+// [E][H/128][I/128] (byte 16*(r%32) + 4*(r/32) + b for row r, 32-block b).
+cudaError_t launch_prepack_w2(const uint8_t* w2, const uint8_t* w2s, int E, int H, int I, int swz, uint8_t* pc,
+                              uint8_t* ps, int num_sms, cudaStream_t st);
 
 // Top-k softmax router over E logits per token (kernels_route.cu).
 constexpr int ROUTE_MAX_EXPERTS = 4096;
@@ -125,15 +129,8 @@ struct StageParams {
   int xs_stride;       // bytes per row of the activation-scale array (as)
   int os_stride;       // stage 1: bytes per row of the output-scale array (os)
   int tile_group;      // many-rows stage 2: N tiles per group of the tile order (<= 0: block-major)
-  // few-rows stage 2 with the finalize folded in (tok_cnt != nullptr): arrival counters
-  // [T][nsl][4] per (token, 256-row slice of H, 32-row quadrant), set by the scatter to
-  // the token's routed pairs; the warp that brings one to zero writes that part of out
-  int* tok_cnt;
-  int nsl;
-  __nv_bfloat16* out;
-  // few-rows kernels: 1 when the sort finished before the preceding kernel began, so the
-  // active-expert list may be read, and the weights loaded, before the wait on that kernel
-  int early_weights;
+  const uint8_t* wpacked;  // few-rows stage 2, prepacked weights: the packed codes (wscale: their scales)
+
   int T, H, I, E, K;
   int act;
   float beta, lbeta;
@@ -161,8 +158,12 @@ cudaError_t swap_set_smem_limits();
 // Shared-memory bytes per operand row (TMA box width) of the few-rows kernels'
 // (kind, stage): the tensor maps the host encodes must use this box width.
 int swap_row_bytes(int kind, int stage);
-cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
-                              int grid, cudaStream_t st);
+// packed (stage 2 only): the weights come prepacked (launch_prepack_w2).
+// ks (stage 1 only): 1, or a split of K over clusters of ks = 2 or 3 CTAs (grid a multiple of ks).
+// swap_split_max_clusters: how many such clusters of the stage-1 kernel fit on the device at once.
+int swap_split_max_clusters(int kind, int ks);
+cudaError_t launch_swap_stage(int kind, int stage, bool packed, int ks, const StageParams& p, const CUtensorMap& tm_w,
+                              const CUtensorMap& tm_x, int grid, cudaStream_t st);
 
 
 }  // namespace moe

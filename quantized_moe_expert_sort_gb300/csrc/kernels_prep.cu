@@ -452,27 +452,12 @@ __device__ __forceinline__ void scatter_units(const __nv_bfloat16* __restrict__ 
   }
 }
 
-// Zero the fp32 combine buffer; set the stage-2 arrival counters of each token
-// to its number of routed pairs (the stage-2 warp that brings a counter to zero
-// writes the token's bf16 row) and write zeros for tokens with none.
-__device__ __forceinline__ void scatter_tail(int T, int H, int K, const int32_t* pair_row, const ScatterOut& so,
-                                             long tid0, long nthreads) {
+// Zero the fp32 combine buffer.
+__device__ __forceinline__ void scatter_tail(int T, int H, const ScatterOut& so, long tid0, long nthreads) {
   if (so.acc32) {
     const long n4 = (long)T * H / 4;
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (long i = tid0; i < n4; i += nthreads) reinterpret_cast<float4*>(so.acc32)[i] = z;
-  }
-  if (so.tok_cnt) {
-    for (long t = tid0; t < T; t += nthreads) {
-      int n = 0;
-      for (int k = 0; k < K; ++k) n += pair_row[t * K + k] >= 0;
-      int* cnt = so.tok_cnt + t * so.nsl * 4;
-      for (int i = 0; i < so.nsl * 4; ++i) cnt[i] = n;
-      if (n == 0) {
-        uint4* o = reinterpret_cast<uint4*>(so.out + t * H);
-        for (int i = 0; i < H / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
   }
 }
 
@@ -483,7 +468,7 @@ __global__ void __launch_bounds__(128) act_scatter_kernel(const __nv_bfloat16* _
   pdl_launch_dependents();
   scatter_units<MODE, CHUNK>(x, T, H, K, pair_row, so, (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5),
                              (long)gridDim.x * (blockDim.x / 32));
-  scatter_tail(T, H, K, pair_row, so, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
+  scatter_tail(T, H, so, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
 }
 
 // L2 prefetch of a contiguous range (16-byte aligned, size % 16 == 0).
@@ -554,7 +539,7 @@ __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t* __res
   pdl_launch_dependents();
   scatter_units<MODE, CHUNK>(x, T, H, K, prow, sc, (long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5),
                              (long)gridDim.x * (blockDim.x / 32));
-  scatter_tail(T, H, K, prow, sc, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
+  scatter_tail(T, H, sc, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
 }
 
 // MXFP4 weight quantisation: fp32 [rows, cols] -> e2m1 codes [rows, cols/2] +

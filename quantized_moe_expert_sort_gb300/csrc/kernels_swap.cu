@@ -93,7 +93,8 @@ template <> struct SwKind<SW_A4> {
 // kind::mxf8f6f4 takes the weights expanded to one 16-element group per 16 bytes
 // (128-byte rows for a K tile of 128), so its tiles take twice the shared memory
 // per HBM byte.
-template <int KIND, int STAGE> struct SwCfg {
+// KS > 1 (stage 1 only): the split-K variant, KS CTAs of a cluster per unit, three operand stages.
+template <int KIND, int STAGE, int KS = 1> struct SwCfg {
   static constexpr bool kNarrow = SwKind<KIND>::kMxf4 && STAGE == 2;
   static constexpr int kKTile = SwKind<KIND>::kMxf4 && !kNarrow ? 256 : 128;
   static constexpr int kChunks = kKTile / 128;                      // 4-block scale chunks per stage
@@ -101,9 +102,10 @@ template <int KIND, int STAGE> struct SwCfg {
   static constexpr int kRow = SwKind<KIND>::kMxf4 ? kKTile / 2 : 128;
   static constexpr int kXStep = SwKind<KIND>::kMxf4 ? kKTile / 2 : kKTile;  // TMA x per stage (bytes / 4-bit elements)
   static constexpr int kKSteps = kRow / 32;                         // MMAs per tile and stage (32 bytes of K each)
-  static constexpr int kNS = kNarrow ? 9 : (SwKind<KIND>::kMxf4 ? 4 : 5);
+  static constexpr int kNS = KS > 1 ? 3 : (kNarrow ? 9 : (SwKind<KIND>::kMxf4 ? 4 : 5));
   static constexpr int kSfRing = kNarrow ? 16 : 8;
-  static constexpr int kSfLag = kNarrow ? 8 : 4;
+  // split-K CTAs run only a few stages each: their scale arrivals may not lag far behind
+  static constexpr int kSfLag = KS > 1 ? 1 : (kNarrow ? 8 : 4);
   static constexpr uint32_t kSwz = kRow == 128 ? tc::SW_128B : tc::SW_64B;
   static constexpr int kSfCols = kChunks == 2 ? 32 : 16;            // TMEM columns per scale slot
 };
@@ -116,8 +118,8 @@ struct UItem {
   int e, tile, row0, nrows;  // nrows < 0: end of work
 };
 
-template <int KIND, int STAGE> struct SwLayout {
-  using C = SwCfg<KIND, STAGE>;
+template <int KIND, int STAGE, int KS = 1> struct SwLayout {
+  using C = SwCfg<KIND, STAGE, KS>;
   static constexpr int kNS = C::kNS;
   static constexpr int kURing = SwKind<KIND>::kURing, kSfRing = C::kSfRing;
   static constexpr uint32_t tile_bytes = 128 * C::kRow;                // one 128-row operand tile
@@ -131,8 +133,11 @@ template <int KIND, int STAGE> struct SwLayout {
   static constexpr uint32_t items = sf + kSfRing * sf_bytes;
   static constexpr uint32_t rows = items + kURing * sizeof(UItem);     // per slot: int tok[kNMax], float w[kNMax]
   static constexpr uint32_t row_bytes = 8 * SwKind<KIND>::kNMax;
-  static constexpr uint32_t bars = rows + kURing * row_bytes;
-  static constexpr uint32_t tmem_slot = bars + (3 * kNS + 4 + 3 * kURing + kSfRing + 1) * 8;
+  // split-K: per partner rank, the g and u partial sums of a 16-row chunk, 128 columns
+  static constexpr uint32_t red = rows + kURing * row_bytes;
+  static constexpr uint32_t red_bytes = (KS - 1) * 16 * 128 * 8;
+  static constexpr uint32_t bars = red + red_bytes;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 4 + 3 * kURing + kSfRing + 1 + (KS > 1 ? 8 : 0)) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;  // + alignment slack
 };
 
@@ -151,6 +156,9 @@ __device__ __forceinline__ void tma_load_2d_sw(void* dst, const CUtensorMap* m, 
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // One arrival on `bar` once every cp.async this thread issued so far has landed
@@ -175,6 +183,62 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* e
   ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
   __syncwarp();
   return ok;
+}
+
+// ---- thread-block cluster helpers (split-K stage 1) ----------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of this CTA's shared-memory location `saddr` in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's earlier
+// writes (including its st.shared::cluster) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Warp-uniform bounded wait for a barrier that other CTAs of the cluster arrive on
+// (acquire at cluster scope: their shared-memory writes are visible afterwards).
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, int* err, volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = global_ns();
+    ok = false;
+    while (true) {
+      if (mbar_try_wait_cluster(bar, parity, MOE_SUSPEND_NS)) { ok = true; break; }
+      if (*abort) break;
+      if (global_ns() - t0 > MOE_WAIT_NS) {
+        *abort = 1;
+        set_error(err, DEV_ERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+// All threads of all CTAs of the cluster (memory ordered at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Requantise one intermediate row y (lane = column j) per 32 along I: kTerms = 1
@@ -221,12 +285,21 @@ template <int KIND, int STAGE> constexpr uint32_t w_tile_tx() {
 
 }  // namespace
 
-template <int KIND, int STAGE>
+// PK (stage 2 only): the weights come prepacked (launch_prepack_w2): the weight map
+// addresses 128-row x 128-element blocks and p.wscale holds 512-byte scale chunks.
+// KS > 1 (stage 1 only): split-K over a cluster of KS CTAs ("Support SiTUv2 in
+// the packed-int4 MoE stage1 epilogue", Technical Details: a split-K stage 1 must
+// carry the SiTUv2 epilogue past its reduction). The CTAs of a cluster run the same
+// items, each over its share of K; ranks 1..KS-1 move their per-row g and u partial
+// sums into rank 0's shared memory (DSMEM), and rank 0 adds them and only then applies
+// the activation and the requantisation -- the activation never sees a partial sum.
+template <int KIND, int STAGE, bool PK, int KS>
 __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(StageParams p, const __grid_constant__ CUtensorMap tm_w,
                                                                    const __grid_constant__ CUtensorMap tm_x) {
   using KD = SwKind<KIND>;
-  using L = SwLayout<KIND, STAGE>;
-  using C = SwCfg<KIND, STAGE>;
+  using L = SwLayout<KIND, STAGE, KS>;
+  using C = SwCfg<KIND, STAGE, KS>;
+  static_assert(KS == 1 || STAGE == 1, "split-K is a stage-1 variant");
   constexpr int kNS = L::kNS;
   constexpr int NMAX = KD::kNMax;
   constexpr int kAccCols = acc_cols<KIND>();
@@ -236,9 +309,8 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   static_assert(kSfRing > kSfLag && L::total <= 232448, "shared memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);  // a stage's TMA copies landed
-  uint64_t* sfull = full + kNS;                                 // a stage's scale chunks landed
-  uint64_t* empty = sfull + kNS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);  // a stage's copies and scale chunks landed
+  uint64_t* empty = full + kNS;
   uint64_t* tfull = empty + kNS;
   uint64_t* tempty = tfull + 2;
   uint64_t* ufull = tempty + 2;
@@ -246,6 +318,8 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   uint64_t* rfull = uempty + kURing;    // the slot's row tokens / weights have landed (stage 2)
   uint64_t* sfempty = rfull + kURing;   // scale-ring slot free (MMA commit)
   uint64_t* drain = sfempty + kSfRing;
+  uint64_t* red_full = drain + 1;   // split-K, rank 0: the partners' partial sums of a chunk (per quadrant)
+  uint64_t* red_empty = red_full + 4;  // split-K, ranks > 0: rank 0 has read this rank's partial sums
   UItem* items = reinterpret_cast<UItem*>(smem + L::items);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem_slot);
   __shared__ int abort_flag;
@@ -260,13 +334,16 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   const int ktiles = (kdim + C::kKTile - 1) / C::kKTile;
   const int nblk_k = kdim / 32;
   const int ntn = STAGE == 1 ? I / 128 : (H + 255) / 256;  // units per expert
+  // split-K: units go to clusters (consecutive CTAs); rank r takes K tiles [ks0, ks1)
+  const int crank = KS > 1 ? (int)cluster_ctarank() : 0;
+  const long cid = KS > 1 ? blockIdx.x / KS : blockIdx.x;
+  const long ncl = KS > 1 ? gridDim.x / KS : gridDim.x;
+  const int ks0 = (ktiles * crank) / KS, ks1 = (ktiles * (crank + 1)) / KS;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // full: the TMA issuer's expect_tx arrive (and the copies' bytes); sfull: the scale
-    // warp's 32 lanes. Kept apart so that the producer can wait for its own copies in
-    // flight before the CTA exits, whatever the other warps did.
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1); mbar_init(&sfull[s], 32); mbar_init(&empty[s], 1); }
+    // full: the TMA issuer's expect_tx arrive (and the copies' bytes) + the scale warp's 32 lanes
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], kEpiWarpsSw); }
     // an item is released by the TMA issuer, the scale warp, the MMA issuer and the epilogue warps
     for (int s = 0; s < kURing; ++s) {
@@ -276,6 +353,11 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
     }
     for (int s = 0; s < kSfRing; ++s) mbar_init(&sfempty[s], 1);
     mbar_init(drain, 1);
+    if (KS > 1)
+      for (int q = 0; q < 4; ++q) {
+        mbar_init(&red_full[q], KS - 1);
+        mbar_init(&red_empty[q], 1);
+      }
     fence_barrier_init();
   }
   if (!KD::kMxf4) {
@@ -291,17 +373,11 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  if (KS > 1) cluster_sync();  // every CTA's barriers are initialised before any remote arrive
   const uint32_t tbase = *tmem_slot;
-  // Everything above overlapped the previous kernel's tail. Without early weights
-  // every thread waits for that kernel here. With them (the sort finished before the
-  // previous kernel began) the item list is read and the weight tiles of the first
-  // stages are loaded at once; only the activation rows, the activation scales and
-  // (through the scale warp's wait) the next kernel's launch wait for it.
-  const bool early = p.early_weights != 0;
-  if (!early) {
-    pdl_wait();
-    pdl_launch_dependents();
-  }
+  // everything above overlapped the previous kernel's tail; its results are read from here on
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 3) {
     // ------------------------------ item scheduler ------------------------------
@@ -310,17 +386,17 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
     const int nunits = p.meta[META_NUM_ACTIVE] * ntn;
     int it = 0;
     bool done = false;
-    long base = blockIdx.x;
-    long u = base + (long)lane * gridDim.x;
+    long base = cid;
+    long u = base + (long)lane * ncl;
     int4 info = u < nunits ? p.active_info[u / ntn] : make_int4(-1, 0, 0, 0);
     while (!done) {
       const int4 cur = info;
       const long cbase = base;
-      base += 32L * gridDim.x;
-      u = base + (long)lane * gridDim.x;
+      base += 32L * ncl;
+      u = base + (long)lane * ncl;
       info = u < nunits ? p.active_info[u / ntn] : make_int4(-1, 0, 0, 0);  // next batch, in flight
       for (int l = 0; l < 32 && !done; ++l) {
-        const long ul = cbase + (long)l * gridDim.x;
+        const long ul = cbase + (long)l * ncl;
         const int el = __shfl_sync(0xFFFFFFFFu, cur.x, l);
         const int cl = __shfl_sync(0xFFFFFFFFu, cur.y, l);
         const int ol = __shfl_sync(0xFFFFFFFFu, cur.z, l);
@@ -390,6 +466,9 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
           const uint8_t* g = p.wscale + ((size_t)nx.e * 2 * I + (size_t)nx.tile * 128) * sb_w;
           bulk_prefetch_l2(g, 128u * sb_w);
           bulk_prefetch_l2(g + (size_t)I * sb_w, 128u * sb_w);
+        } else if (PK) {  // the item's chunks: tiles 2 tile, 2 tile + 1, all K chunks, contiguous
+          const int ht0 = 2 * nx.tile, nt = min(2, H / 128 - ht0), kcn = I / 128;
+          bulk_prefetch_l2(p.wscale + ((size_t)nx.e * (H / 128) + ht0) * kcn * 512, (uint32_t)(nt * kcn * 512));
         } else {
           const int rows = min(256, H - nx.tile * 256);
           bulk_prefetch_l2(p.wscale + ((size_t)nx.e * H + (size_t)nx.tile * 256) * sb_w, (uint32_t)rows * sb_w);
@@ -401,21 +480,6 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
       uint32_t stage = 0;
       int it = 0;
       bool ok = true;
-      // activation-row loads of stages armed before the wait on the previous kernel
-      struct Deferred { int slot, kx, row, nbox; };
-      Deferred def[kNS];
-      int ndef = 0;
-      bool dep = !early;
-      auto flush_deferred = [&]() {
-        pdl_wait();
-        for (int i = 0; i < ndef; ++i) {
-          uint8_t* sb = smem + L::b + def[i].slot * L::b_bytes;
-          for (int bx = 0; bx < def[i].nbox; ++bx)
-            tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, def[i].kx, def[i].row + 16 * bx, &full[def[i].slot]);
-        }
-        ndef = 0;
-        dep = true;
-      };
       while (ok) {
         const int us = it % kURing;
         if (!mbar_wait_or_abort(&ufull[us], (it / kURing) & 1, p.err, &abort_flag)) break;
@@ -427,34 +491,46 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
         const int nsub = ui.nrows * KD::kTerms;  // B rows: the item's sub-rows
         const int nbox = (nsub + 15) / 16;
         const uint32_t btx = (uint32_t)nbox * 16 * C::kRow;
-        for (int ks = 0; ks < ktiles; ++ks, ++stage) {
+        for (int ks = ks0; ks < ks1; ++ks, ++stage) {
           const int slot = stage % kNS;
-          if (!dep && ndef == kNS) flush_deferred();  // the ring is full of weight-only stages
           if (!mbar_wait_or_abort(&empty[slot], ((stage / kNS) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
           uint8_t* sa = smem + L::a + slot * L::a_bytes;
           uint8_t* sb = smem + L::b + slot * L::b_bytes;
-          mbar_arrive_expect_tx(&full[slot], 2 * w_tile_tx<KIND, STAGE>() + btx);
           const int kx = ks * C::kXStep;
-          if (STAGE == 1) {
-            tma_load_4d(sa, &tm_w, kx, ui.tile * 128, 0, ui.e, &full[slot]);
-            tma_load_4d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 128, 1, ui.e, &full[slot]);
-          } else {  // rows past H (odd H / 128) are filled with zeros
-            tma_load_3d(sa, &tm_w, kx, ui.tile * 256, ui.e, &full[slot]);
-            tma_load_3d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 256 + 128, ui.e, &full[slot]);
+          if (PK) {
+            // one contiguous 8 KB block per 128-row tile; a second tile past H (odd H / 128)
+            // is not loaded (its rows are never stored). kind::mxf4: the block is stored
+            // pre-swizzled, one bulk copy; kind::mxf8f6f4: the unpacking TMA.
+            const int ht0 = 2 * ui.tile, kcn = I / 128;
+            const bool two = ht0 + 1 < H / 128;
+            mbar_arrive_expect_tx(&full[slot], (two ? 2 : 1) * w_tile_tx<KIND, STAGE>() + btx);
+            const int y0 = ((ui.e * (H / 128) + ht0) * kcn + ks) * 128;
+            if (KD::kMxf4) {
+              bulk_g2s(sa, p.wpacked + (size_t)y0 * 64, 8192u, &full[slot]);
+              if (two) bulk_g2s(sa + L::tile_bytes, p.wpacked + (size_t)(y0 + kcn * 128) * 64, 8192u, &full[slot]);
+            } else {
+              tma_load_2d_sw(sa, &tm_w, 0, y0, &full[slot]);
+              if (two) tma_load_2d_sw(sa + L::tile_bytes, &tm_w, 0, y0 + kcn * 128, &full[slot]);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[slot], 2 * w_tile_tx<KIND, STAGE>() + btx);
+            if (STAGE == 1) {
+              tma_load_4d(sa, &tm_w, kx, ui.tile * 128, 0, ui.e, &full[slot]);
+              tma_load_4d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 128, 1, ui.e, &full[slot]);
+            } else {  // rows past H (odd H / 128) are filled with zeros
+              tma_load_3d(sa, &tm_w, kx, ui.tile * 256, ui.e, &full[slot]);
+              tma_load_3d(sa + L::tile_bytes, &tm_w, kx, ui.tile * 256 + 128, ui.e, &full[slot]);
+            }
           }
           // routed rows: contiguous sub-rows [row0 * kTerms, (row0 + nrows) * kTerms), 16-row boxes
           // (rows past this expert belong to later experts and only fill unused columns)
-          if (dep) {
-            for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, kx, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
-          } else {
-            def[ndef++] = Deferred{slot, kx, ui.row0 * KD::kTerms, nbox};
-          }
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d_sw(sb + bx * 16 * C::kRow, &tm_x, kx, ui.row0 * KD::kTerms + 16 * bx, &full[slot]);
         }
       }
-      if (!dep) flush_deferred();  // fewer stages than the ring holds (or an early end)
       // every copy this thread started has landed before the CTA may exit (after an
-      // abort nobody else waits for them); in a normal run these return at once
+      // abort nobody else waits for them): in a normal run these phases completed long
+      // ago; after an abort the bounded wait outlasts any copy in flight
       for (uint32_t g = stage > (uint32_t)kNS ? stage - kNS : 0u; g < stage; ++g)
         mbar_wait(&full[g % kNS], (g / kNS) & 1, p.err);
     }
@@ -464,10 +540,6 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
     // g - kSfRing); warp 1 arrives on the operand slot's full barrier kSfLag stages
     // later, once its copies have landed, after checking that the operand slot
     // has been re-armed for that stage.
-    if (early) {  // activation scales come from the previous kernel
-      pdl_wait();
-      pdl_launch_dependents();
-    }
     const int sb_w = kdim / 32;  // weight-scale bytes per row
     uint32_t stage = 0, pend = 0;
     int it = 0;
@@ -476,7 +548,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
       const uint32_t g = stage - pend;
       // the operand slot of stage g is in g's phase once the MMA released stage g - kNS
       ok = ok && warp_wait(&empty[g % kNS], ((g / kNS) & 1) ^ 1, p.err, &abort_flag);
-      mbar_arrive(&sfull[g % kNS]);
+      mbar_arrive(&full[g % kNS]);
       --pend;
     };
     while (ok) {
@@ -494,18 +566,25 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
                                        : p.wscale + ((size_t)ui.e * H + (size_t)ui.tile * 256) * sb_w;
       const size_t w1 = STAGE == 1 ? (size_t)I : 128;
       const bool t1 = STAGE == 1 || ui.tile * 256 + 128 < H;  // second tile inside the matrix
-      for (int ks = 0; ks < ktiles && ok; ++ks) {
+      for (int ks = ks0; ks < ks1 && ok; ++ks) {
         const int fslot = stage % kSfRing;
         if (!warp_wait(&sfempty[fslot], ((stage / kSfRing) & 1) ^ 1, p.err, &abort_flag)) { ok = false; break; }
         uint8_t* sf = smem + L::sf + fslot * L::sf_bytes;  // [sfa tile 0 | sfa tile 1 | sfb], sf_op bytes each
         for (int c = 0; c < C::kChunks; ++c) {
           const int kb0 = ks * C::kBlocks + 4 * c;
           if (kb0 < nblk_k) {  // kdim % 128 == 0: a chunk is all in or all out
+            if (PK) {  // the chunk is stored as it lands: 16 bytes per lane
+              const uint8_t* pk = p.wscale + ((size_t)ui.e * (H / 128) + 2 * ui.tile) * (I / 128) * 512 +
+                                  (size_t)(kb0 / 4) * 512 + 16 * lane;
+              cp_async16(sf + 512 * c + 16 * lane, pk);
+              if (t1) cp_async16(sf + L::sf_op + 512 * c + 16 * lane, pk + (size_t)(I / 128) * 512);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int m = 4 * lane + i;
-              cp_async4(sf + 512 * c + sf_off_sw(m), wsrc + (size_t)m * sb_w + kb0);
-              if (t1) cp_async4(sf + L::sf_op + 512 * c + sf_off_sw(m), wsrc + (w1 + m) * sb_w + kb0);
+              for (int i = 0; i < 4; ++i) {
+                const int m = 4 * lane + i;
+                cp_async4(sf + 512 * c + sf_off_sw(m), wsrc + (size_t)m * sb_w + kb0);
+                if (t1) cp_async4(sf + L::sf_op + 512 * c + sf_off_sw(m), wsrc + (w1 + m) * sb_w + kb0);
+              }
             }
             for (int n = lane; n < nsub; n += 32)
               cp_async4(sf + 2 * L::sf_op + 512 * c + sf_off_sw(n), p.as + (sub0 + n) * p.xs_stride + kb0);
@@ -560,9 +639,8 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
                                        : tc::idesc_bs(128, nmma, tc::F8F6F4_E2M1, tc::F8F6F4_E4M3, 0, 0);
         const uint32_t dg = tbase + buf * 2 * kAccCols;
         bool ok = true;
-        for (int ks = 0; ks < ktiles; ++ks) {
-          if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag) ||
-              !mbar_wait_or_abort(&sfull[slot], phase, p.err, &abort_flag)) {
+        for (int ks = ks0; ks < ks1; ++ks) {
+          if (!mbar_wait_or_abort(&full[slot], phase, p.err, &abort_flag)) {
             ok = false;
             break;
           }
@@ -583,7 +661,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
 #pragma unroll
           for (int i = 0; i < C::kKSteps; ++i) {
             if (i > 0 && i * (C::kKTile / C::kKSteps) >= kleft) break;  // K steps past the end of K
-            const uint32_t acc = (ks > 0 || i > 0) ? 1u : 0u;
+            const uint32_t acc = (ks > ks0 || i > 0) ? 1u : 0u;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
               const uint64_t dai = da + ((g * L::tile_bytes + 32 * i) >> 4);
@@ -620,6 +698,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
     const int wg = (warp - 4) / kEpiWarpsSw;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     int tok_a = 0, tok_b = 0;
+    int red_cnt = 0;  // split-K: chunks exchanged so far (barrier phases)
     float w_a = 0.0f, w_b = 0.0f;
     int it = wg;
     while (true) {
@@ -691,15 +770,58 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
 #pragma unroll
           for (int n = 0; n < 16; ++n)
             if (n < nn)
-              requant_row<KD::kTerms, KD::kMxf4>(act_apply(p.act, gv[n], uv[n], p.beta, p.lbeta), row0 + c0 + n, j,
+              requant_row<KD::kTerms, KD::kMxf4>(act_apply<(KD::kTerms > 1)>(p.act, gv[n], uv[n], p.beta, p.lbeta), row0 + c0 + n, j,
                                                  lane, I, p.oq, p.os, p.os_stride);
         };
-        for (int c0 = 0; c0 < nrows; c0 += 16) {
+        bool ok = true;
+        for (int c0 = 0; c0 < nrows && ok; c0 += 16) {
           float gv[16], uv[16];
           load_pair(dg, dg + kAccCols, c0, gv, uv);
           release_acc(c0);
+          if (KS > 1 && ks0 == ks1) {  // an empty K share (the host avoids it): a zero partial
+#pragma unroll
+            for (int n = 0; n < 16; ++n) { gv[n] = 0.0f; uv[n] = 0.0f; }
+          }
+          if (KS > 1) {
+            const int nn = min(16, nrows - c0);
+            // (n, column 32 q + lane) of rank r's partial sums: float2 at red + ((r-1) * 16 + n) * 1024 + 8 * col
+            const uint32_t col8 = 8u * (32 * q + lane);
+            if (crank != 0) {
+              // the previous chunk's partial sums must have been read before this chunk overwrites them
+              if (red_cnt > 0 && !warp_wait_cluster(&red_empty[q], (red_cnt - 1) & 1, p.err, &abort_flag)) {
+                ok = false;
+                break;
+              }
+              const uint32_t dst = mapa_shared(smem_u32(smem + L::red) + (uint32_t)(crank - 1) * 16 * 1024 + col8, 0);
+#pragma unroll
+              for (int n = 0; n < 16; ++n)
+                if (n < nn) st_cluster_v2(dst + n * 1024, gv[n], uv[n]);
+              __syncwarp();
+              if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&red_full[q]), 0));
+              ++red_cnt;
+              continue;  // rank 0 finishes the chunk
+            }
+            if (!warp_wait_cluster(&red_full[q], red_cnt & 1, p.err, &abort_flag)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int r = 1; r < KS; ++r)
+#pragma unroll
+              for (int n = 0; n < 16; ++n)
+                if (n < nn) {
+                  const float2 v = *reinterpret_cast<const float2*>(smem + L::red + ((r - 1) * 16 + n) * 1024 + col8);
+                  gv[n] += v.x;
+                  uv[n] += v.y;
+                }
+            __syncwarp();
+            if (lane == 0)
+              for (int r = 1; r < KS; ++r) mbar_arrive_remote(mapa_shared(smem_u32(&red_empty[q]), r));
+            ++red_cnt;
+          }
           requant_rows(c0, gv, uv);
         }
+        if (!ok) break;
       } else {
         const int h0 = ui.tile * 256 + 32 * q + lane;  // rows of H of this lane in tiles 0 and 1
         const bool h1ok = h0 + 128 < H;
@@ -719,31 +841,6 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
               if (h1ok) atomicAdd(dst + 128, w * v1[n]);
             }
           }
-          if (p.tok_cnt) {
-            // Finalize folded in: each row counts its arrival on its token's counter for
-            // this (slice, quadrant); the warp that brings a counter to zero holds the last
-            // contribution and writes those 32 + 32 values of out as bf16 (RNE).
-            __threadfence();  // this warp's adds are performed before they are counted
-            const int col = c0 + lane;
-            const int ta = __shfl_sync(0xFFFFFFFFu, tok_a, col & 31);
-            const int tb = __shfl_sync(0xFFFFFFFFu, tok_b, col & 31);
-            const int tl = col < 32 ? ta : tb;
-            bool last = false;
-            if (lane < nn) last = atomicSub(p.tok_cnt + ((size_t)tl * p.nsl + ui.tile) * 4 + q, 1) == 1;
-            unsigned done = __ballot_sync(0xFFFFFFFFu, last);
-            if (done) {
-              __threadfence();  // the other contributors' adds are visible from here on
-              while (done) {
-                const int n = __ffs(done) - 1;
-                done &= done - 1;
-                const int t = __shfl_sync(0xFFFFFFFFu, tl, n);
-                const float* src = p.acc32 + (size_t)t * H + h0;
-                __nv_bfloat16* o = p.out + (size_t)t * H + h0;
-                o[0] = __float2bfloat16_rn(__ldcg(src));
-                if (h1ok) o[128] = __float2bfloat16_rn(__ldcg(src + 128));
-              }
-            }
-          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&uempty[us]);  // the row values have been consumed
@@ -752,6 +849,7 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
   }
   tc::fence_before();
   __syncthreads();
+  if (KS > 1) cluster_sync();  // no CTA leaves while a partner may still touch its shared memory
   if (warp == 2) {
     __syncwarp();
     tc::fence_after();
@@ -760,10 +858,20 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
 }
 
 // ---------------------------------------------------------------------------
-template <int KIND, int STAGE>
+template <int KIND, int STAGE, bool PK, int KS>
+static cudaError_t set_limit_one() {
+  return cudaFuncSetAttribute(swap_stage_kernel<KIND, STAGE, PK, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)SwLayout<KIND, STAGE, KS>::total);
+}
+
+template <int KIND>
 static cudaError_t set_limit_sw() {
-  return cudaFuncSetAttribute(swap_stage_kernel<KIND, STAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)SwLayout<KIND, STAGE>::total);
+  cudaError_t e = set_limit_one<KIND, 1, false, 1>();
+  if (e == cudaSuccess) e = set_limit_one<KIND, 1, false, 2>();
+  if (e == cudaSuccess) e = set_limit_one<KIND, 1, false, 3>();
+  if (e == cudaSuccess) e = set_limit_one<KIND, 2, false, 1>();
+  if (e == cudaSuccess) e = set_limit_one<KIND, 2, true, 1>();
+  return e;
 }
 
 int swap_row_bytes(int kind, int stage) {
@@ -773,30 +881,81 @@ int swap_row_bytes(int kind, int stage) {
 }
 
 cudaError_t swap_set_smem_limits() {
-  cudaError_t e = set_limit_sw<SW_A16, 1>();
-  if (e == cudaSuccess) e = set_limit_sw<SW_A16, 2>();
-  if (e == cudaSuccess) e = set_limit_sw<SW_A8, 1>();
-  if (e == cudaSuccess) e = set_limit_sw<SW_A8, 2>();
-  if (e == cudaSuccess) e = set_limit_sw<SW_A4, 1>();
-  if (e == cudaSuccess) e = set_limit_sw<SW_A4, 2>();
+  cudaError_t e = set_limit_sw<SW_A16>();
+  if (e == cudaSuccess) e = set_limit_sw<SW_A8>();
+  if (e == cudaSuccess) e = set_limit_sw<SW_A4>();
   return e;
 }
 
-template <int KIND>
-static cudaError_t launch_sw(int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
-                             int grid, cudaStream_t st) {
-  if (stage == 1)
-    return launch_k(swap_stage_kernel<KIND, 1>, dim3(grid), dim3(threads_sw<1>()), SwLayout<KIND, 1>::total, st, true, p, tm_w,
-                    tm_x);
-  return launch_k(swap_stage_kernel<KIND, 2>, dim3(grid), dim3(threads_sw<2>()), SwLayout<KIND, 2>::total, st, true, p, tm_w,
-                  tm_x);
+// Split-K launch: clusters of KS consecutive CTAs, with programmatic dependent launch.
+template <int KIND, int KS>
+static cudaError_t launch_split(const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x, int grid,
+                                cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads_sw<1>());
+  cfg.dynamicSmemBytes = SwLayout<KIND, 1, KS>::total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = KS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, swap_stage_kernel<KIND, 1, false, KS>, p, tm_w, tm_x);
 }
 
-cudaError_t launch_swap_stage(int kind, int stage, const StageParams& p, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
-                              int grid, cudaStream_t st) {
-  if (kind == SW_A16) return launch_sw<SW_A16>(stage, p, tm_w, tm_x, grid, st);
-  if (kind == SW_A8) return launch_sw<SW_A8>(stage, p, tm_w, tm_x, grid, st);
-  return launch_sw<SW_A4>(stage, p, tm_w, tm_x, grid, st);
+template <int KIND>
+static cudaError_t launch_sw(int stage, bool packed, int ks, const StageParams& p, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_x, int grid, cudaStream_t st) {
+  if (stage == 1) {
+    if (ks == 3) return launch_split<KIND, 3>(p, tm_w, tm_x, grid, st);
+    if (ks == 2) return launch_split<KIND, 2>(p, tm_w, tm_x, grid, st);
+    return launch_k(swap_stage_kernel<KIND, 1, false, 1>, dim3(grid), dim3(threads_sw<1>()), SwLayout<KIND, 1>::total,
+                    st, true, p, tm_w, tm_x);
+  }
+  if (packed)
+    return launch_k(swap_stage_kernel<KIND, 2, true, 1>, dim3(grid), dim3(threads_sw<2>()), SwLayout<KIND, 2>::total, st,
+                    true, p, tm_w, tm_x);
+  return launch_k(swap_stage_kernel<KIND, 2, false, 1>, dim3(grid), dim3(threads_sw<2>()), SwLayout<KIND, 2>::total, st,
+                  true, p, tm_w, tm_x);
+}
+
+template <int KIND, int KS>
+static int max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(KS * 64);
+  cfg.blockDim = dim3(threads_sw<1>());
+  cfg.dynamicSmemBytes = SwLayout<KIND, 1, KS>::total;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, swap_stage_kernel<KIND, 1, false, KS>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int swap_split_max_clusters(int kind, int ks) {
+  if (kind == SW_A16) return ks == 3 ? max_clusters<SW_A16, 3>() : max_clusters<SW_A16, 2>();
+  if (kind == SW_A8) return ks == 3 ? max_clusters<SW_A8, 3>() : max_clusters<SW_A8, 2>();
+  return ks == 3 ? max_clusters<SW_A4, 3>() : max_clusters<SW_A4, 2>();
+}
+
+cudaError_t launch_swap_stage(int kind, int stage, bool packed, int ks, const StageParams& p, const CUtensorMap& tm_w,
+                              const CUtensorMap& tm_x, int grid, cudaStream_t st) {
+  if (kind == SW_A16) return launch_sw<SW_A16>(stage, packed, ks, p, tm_w, tm_x, grid, st);
+  if (kind == SW_A8) return launch_sw<SW_A8>(stage, packed, ks, p, tm_w, tm_x, grid, st);
+  return launch_sw<SW_A4>(stage, packed, ks, p, tm_w, tm_x, grid, st);
 }
 
 }  // namespace moe

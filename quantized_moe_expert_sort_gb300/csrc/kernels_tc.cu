@@ -88,7 +88,7 @@ struct TcLayout {
   static constexpr uint32_t epi = ws + 2 * ws_bytes;               // stage-2 transpose: per epilogue warp 32 x 36 fp32
   static constexpr uint32_t epi_bytes = 32 * 36 * 4;
   static constexpr uint32_t bars = epi + kEpiWarps * epi_bytes;
-  static constexpr uint32_t tmem_slot = bars + (3 * kNS + 8) * 8;
+  static constexpr uint32_t tmem_slot = bars + (2 * kNS + 8) * 8;
   static constexpr uint32_t total = tmem_slot + 16 + 1024;        // + alignment slack
 };
 
@@ -120,9 +120,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
   using KD = Kind<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);  // a stage's TMA copies landed
-  uint64_t* sfull = full + kNS;                                        // a stage's weight scales transposed
-  uint64_t* empty = sfull + kNS;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);  // a stage's copies and scales are ready
+  uint64_t* empty = full + kNS;
   uint64_t* tfull = empty + kNS;
   uint64_t* tempty = tfull + 2;
   uint64_t* wsfull = tempty + 2;   // weight scales of a tile landed in staging
@@ -146,10 +145,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // full: the TMA issuer's expect_tx arrive (and the copies' bytes); sfull: the 32
-    // scale-transpose lanes. Kept apart so that a producer can wait for its own
-    // copies in flight, whatever the other warps did.
-    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1); mbar_init(&sfull[s], 32); mbar_init(&empty[s], 1); }
+    // full: the TMA issuer's expect_tx arrive (and the copies' bytes) + the 32 scale-transpose lanes
+    for (int s = 0; s < kNS; ++s) { mbar_init(&full[s], 1 + 32); mbar_init(&empty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], kEpiWarps);
@@ -229,7 +226,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
       // Before the CTA may exit, every copy this thread started must have landed
       // (after an abort the consumers no longer wait for them): the last kNS
       // operand stages and the last two scale stagings. In a normal run these
-      // phases completed long ago and the waits return at once.
+      // phases completed long ago and the waits return at once; after an abort the
+      // bounded wait outlasts any copy in flight.
       for (uint32_t g = stage > (uint32_t)kNS ? stage - kNS : 0u; g < stage; ++g)
         mbar_wait(&full[g % kNS], (g / kNS) & 1, p.err);
       for (int l = lt > 2 ? lt - 2 : 0; l < lt; ++l) mbar_wait(&wsfull[l & 1], (l >> 1) & 1, p.err);
@@ -263,7 +261,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           }
         }
         fence_proxy_async();  // generic smem writes -> visible to tcgen05.cp
-        mbar_arrive(&sfull[slot]);
+        mbar_arrive(&full[slot]);
       }
       __syncwarp();
       if (!ok) break;
@@ -291,8 +289,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
         for (int ks = 0; ks < ktiles; ++ks, ++stage) {
           const int slot = stage % kNS;
           // an aborted wait leaves the stage unread: no MMA runs on operands that never landed
-          if (!mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag) ||
-              !mbar_wait_or_abort(&sfull[slot], (stage / kNS) & 1, p.err, &abort_flag)) {
+          if (!mbar_wait_or_abort(&full[slot], (stage / kNS) & 1, p.err, &abort_flag)) {
             ok = false;
             break;
           }
@@ -364,7 +361,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            y[i] = act_apply(p.act, __uint_as_float(gr[i]), __uint_as_float(ur[i]), p.beta, p.lbeta);
+            y[i] = act_apply<false>(p.act, __uint_as_float(gr[i]), __uint_as_float(ur[i]), p.beta, p.lbeta);
             amax = fmaxf(amax, fabsf(y[i]));
           }
           if (valid) {

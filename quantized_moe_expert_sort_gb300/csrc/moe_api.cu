@@ -93,10 +93,14 @@ struct moe_ctx {
   int tc_min_rows;  // mean routed rows per active expert from which the tcgen05 path is used
   int tc_group;     // many-rows stage 2: N tiles per group of the tile order (0: chosen per call)
   int fused;        // 1: sort + scatter in one launch (calls of up to SORT_SMALL_MAX_PAIRS pairs)
-  int fold;         // 1: the few-rows stage 2 writes out itself (no finalize launch)
-  int early;        // 1: the few-rows stages load weights before waiting on their predecessor
-  int nsl;          // 256-row slices of H (stage-2 arrival counters)
-  int* tok_cnt;     // [max_tokens][nsl][4] stage-2 arrival counters
+  int split_k;      // 1: few-rows stage 1 splits K over clusters when its units fill few SMs
+  int split_cap[3][4];  // [kind][ks]: clusters of the split stage-1 kernel resident at once (0: unknown)
+  // prepacked stage-2 weights (moe_prepack): used when moe_forward's w2 is pk_src
+  const uint8_t* pk_src;
+  int pk_adt;  // the a_dtype whose few-rows stage 2 the packed copy serves
+  uint8_t* pk_codes;
+  uint8_t* pk_scales;
+  const void* tm_w2pk_key; int tm_w2pk_kind; CUtensorMap tm_w2pk;
   int last_inter_layout;
   int last_tile_m;
   // profiling (moe_set_profiling)
@@ -117,7 +121,7 @@ static void free_ctx(moe_ctx* c) {
   void* ptrs[] = {c->sorted_ids, c->block_expert, c->expert_count, c->expert_offset, c->active_experts,
                   c->meta, c->hist, c->xq, c->xs, c->inter_q, c->inter_s, c->acc32, c->err,
                   c->xq_sorted, c->xs_sorted, c->pair_row, c->row_tok, c->row_w, c->active_info,
-                  c->st_x, c->st_ids, c->st_w, c->st_out, c->tok_cnt};
+                  c->st_x, c->st_ids, c->st_w, c->st_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (cudaEvent_t e : c->ev)
@@ -213,6 +217,31 @@ static moe_status make_w13sw_map(moe_ctx* c, const uint8_t* w13, int kind) {
   return MOE_OK;
 }
 
+// Prepacked w2 (kernels_pack.cu): rows of 64 bytes (one 128-element K chunk), each
+// 128 consecutive rows one (expert, 128-row tile, K chunk) block; unpacked by TMA
+// to 128-byte rows for kind::mxf8f6f4.
+static moe_status make_w2pk_map(moe_ctx* c, int kind) {
+  if (c->tm_w2pk_key == c->pk_codes && c->tm_w2pk_kind == kind) return MOE_OK;
+  const cuuint64_t rows = (cuuint64_t)c->E * (c->H / 128) * (c->I / 128) * 128;
+  cuuint64_t strides[1] = {64};
+  moe_status s;
+  if (kind == TC_A8W4) {
+    cuuint64_t dims[2] = {128, rows};
+    cuuint32_t box[2] = {128, 128};
+    s = encode(&c->tm_w2pk, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, c->pk_codes, dims, strides, box,
+               CU_TENSOR_MAP_SWIZZLE_128B, "prepacked w2, unpacked");
+  } else {
+    cuuint64_t dims[2] = {64, rows};
+    cuuint32_t box[2] = {64, 128};
+    s = encode(&c->tm_w2pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c->pk_codes, dims, strides, box,
+               CU_TENSOR_MAP_SWIZZLE_64B, "prepacked w2");
+  }
+  if (s != MOE_OK) return s;
+  c->tm_w2pk_key = c->pk_codes;
+  c->tm_w2pk_kind = kind;
+  return MOE_OK;
+}
+
 static SortOut sort_out(moe_ctx* c) {
   SortOut so;
   so.sorted_ids = c->sorted_ids;
@@ -282,7 +311,6 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   c->cap_blocks = c->cap_rows;  // enough for tile_m = 1
   c->hist_chunks = (int)((pairs + SORT_CHUNK - 1) / SORT_CHUNK);
   if (c->hist_chunks < 1) c->hist_chunks = 1;
-  c->nsl = (H + 255) / 256;
 
   struct { void** p; size_t bytes; } allocs[] = {
       {(void**)&c->sorted_ids, sizeof(int32_t) * c->cap_rows},
@@ -308,7 +336,6 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
       {(void**)&c->st_ids, sizeof(int32_t) * pairs},
       {(void**)&c->st_w, sizeof(float) * pairs},
       {(void**)&c->st_out, (size_t)max_tokens * H * 2},
-      {(void**)&c->tok_cnt, sizeof(int) * (size_t)max_tokens * c->nsl * 4},
   };
   const long inject = g_fail_alloc.exchange(-1);
   long idx = 0;
@@ -336,10 +363,8 @@ moe_status moe_create(moe_ctx** out, int H, int I, int E, int K, int max_tokens,
   if (const char* v = getenv("MOE_TC_GROUP")) c->tc_group = atoi(v);
   c->fused = 0;
   if (const char* v = getenv("MOE_FUSED")) c->fused = atoi(v);
-  c->fold = 0;
-  if (const char* v = getenv("MOE_FOLD")) c->fold = atoi(v);
-  c->early = 1;
-  if (const char* v = getenv("MOE_EARLY")) c->early = atoi(v);
+  c->split_k = 1;
+  if (const char* v = getenv("MOE_SPLITK")) c->split_k = atoi(v);
   c->last_inter_stride = scale_row_stride(I);
   *out = c;
   return MOE_OK;
@@ -413,6 +438,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   const bool use_tc = adt != MOE_A_BF16 && c->tc_min_rows > 0 && pairs >= (long)c->tc_min_rows * max_active &&
                       c->H <= TC_MAX_K && c->I <= TC_MAX_K;
   const bool use_sw = !use_tc;
+  const bool use_packed = use_sw && c->pk_codes && c->pk_src == w2 && c->pk_adt == adt;
   const int tile_m = use_tc ? TC_TILE_M : 1;
   const int kind = adt == MOE_A_FP8 ? TC_A8W4 : TC_A4W4;
   const int swkind = adt == MOE_A_BF16 ? SW_A16 : (adt == MOE_A_FP8 ? SW_A8 : SW_A4);
@@ -444,9 +470,14 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     ms = make_w13sw_map(c, w13, wkind);
     if (ms != MOE_OK) return ms;
     // stage 2 streams K = inter in the kernel's row width: 64-byte rows take the
-    // packed 64-byte-box map, 128-byte rows the 128-byte one (unpacked for A8)
+    // packed 64-byte-box map, 128-byte rows the 128-byte one (unpacked for A8);
+    // a prepacked copy of these weights takes its own map
     const bool narrow2 = swap_row_bytes(swkind, 2) == 64;
-    ms = narrow2 ? make_w2sw_map(c, w2) : make_w2tc_map(c, w2, wkind);
+    if (use_packed) {
+      ms = make_w2pk_map(c, wkind);
+    } else {
+      ms = narrow2 ? make_w2sw_map(c, w2) : make_w2tc_map(c, w2, wkind);
+    }
     if (ms != MOE_OK) return ms;
     cuuint32_t box[2] = {128, 16};
     cuuint32_t ibox[2] = {narrow2 ? 64u : 128u, 16};
@@ -466,9 +497,6 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   c->last_tile_m = tile_m;
   c->last_inter_layout = use_tc ? 1 : (adt == MOE_A_BF16 ? 2 : 0);
   c->last_inter_stride = use_sw ? is_sw : scale_row_stride(c->I);
-  // the few-rows stage 2 writes out itself (arrival counters); the many-rows one
-  // leaves the fp32 sum for the finalize kernel
-  const bool fold = use_sw && c->fold;
   ScatterOut sc{};
   sc.codes = c->xq_sorted;
   sc.scales = c->xs_sorted;
@@ -478,11 +506,6 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     sc.topk_w = w;
     sc.row_tok = c->row_tok;
     sc.row_w = c->row_w;
-  }
-  if (fold) {
-    sc.tok_cnt = c->tok_cnt;
-    sc.nsl = c->nsl;
-    sc.out = static_cast<__nv_bfloat16*>(out);
   }
   cudaError_t e;
   const bool one_launch = c->fused && pairs <= SORT_SMALL_MAX_PAIRS;  // sort + scatter fused
@@ -524,12 +547,16 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
 
   if (use_tc) {
     long t1 = max_blocks * (c->I / 64), t2 = max_blocks * (c->H / 128);
-    // Stage-2 tile order: block-major while the fp32 combine buffer fits in L2 with
-    // room to spare; beyond that, N tiles in groups whose slice of the buffer
-    // (T x 128 columns x 4 bytes per N tile) stays near 48 MB.
+    // Stage-2 tile order: block-major keeps each 128-row block of the intermediate in
+    // L2 while its N tiles run, and scatters into the fp32 combine buffer; N tiles in
+    // groups (the buffer's slice T x 128 x 4 bytes per N tile near 48 MB) keep the
+    // buffer's active part in L2 but read the intermediate once per group. Groups pay
+    // off when the buffer exceeds L2 and is larger than the intermediate they re-read.
     const double acc_bytes = (double)T * c->H * 4.0, slice = (double)T * 128 * 4.0;
-    p2.tile_group = acc_bytes <= 64.0 * (1 << 20) ? 0 : (int)(48.0 * (1 << 20) / slice);
-    if (acc_bytes > 64.0 * (1 << 20) && p2.tile_group < 1) p2.tile_group = 1;
+    const double inter_bytes = (double)pairs * c->I * (adt == MOE_A_FP8 ? 1.0 + 1.0 / 32 : 0.5 + 1.0 / 32);
+    const bool grouped = acc_bytes > 64.0 * (1 << 20) && acc_bytes > 2.0 * inter_bytes;
+    p2.tile_group = grouped ? (int)(48.0 * (1 << 20) / slice) : 0;
+    if (grouped && p2.tile_group < 1) p2.tile_group = 1;
     if (c->tc_group > 0) p2.tile_group = c->tc_group;
     prof_mark(c, st, "stage1");
     StageParams q1 = p1;
@@ -547,32 +574,40 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     q1.as = c->xs_sorted;
     q1.xs_stride = xs_sw;
     q1.os_stride = is_sw;
-    q1.early_weights = c->early && !one_launch;  // the sort is two kernels back
     prof_mark(c, st, "stage1");
     const long u1 = max_active * (c->I / 128);
-    e = launch_swap_stage(swkind, 1, q1, c->tm_w13sw, tm_xs, (int)(u1 < c->num_sms ? u1 : c->num_sms), st);
+    // split K over clusters of ks CTAs when the units leave most SMs idle (a few tokens)
+    const int kt1 = c->H / (adt == MOE_A_FP8 ? 128 : 256);  // stage-1 K tiles
+    // split only when one wave of resident clusters holds every unit (clusters need ks
+    // free SMs of one GPC each, so fewer fit than num_sms / ks)
+    auto cap = [&](int k) {
+      if (!c->split_cap[swkind][k]) c->split_cap[swkind][k] = 1 + swap_split_max_clusters(swkind, k);
+      return (long)c->split_cap[swkind][k] - 1;
+    };
+    int ks = 1;
+    if (c->split_k && kt1 >= 3 && u1 <= cap(3)) ks = 3;
+    else if (c->split_k && kt1 >= 2 && u1 <= cap(2)) ks = 2;
+    const long g1 = ks > 1 ? u1 * ks : (u1 < c->num_sms ? u1 : c->num_sms);
+    e = launch_swap_stage(swkind, 1, false, ks, q1, c->tm_w13sw, tm_xs, (int)g1, st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     StageParams q2 = p2;
     q2.xs_stride = is_sw;
     q2.row_tok = c->row_tok;
     q2.row_w = c->row_w;
-    q2.early_weights = c->early;  // the sort and the scatter are at least two kernels back
-    if (fold) {
-      q2.tok_cnt = c->tok_cnt;
-      q2.nsl = c->nsl;
-      q2.out = static_cast<__nv_bfloat16*>(out);
+    if (use_packed) {
+      q2.wscale = c->pk_scales;
+      q2.wpacked = c->pk_codes;
     }
     prof_mark(c, st, "stage2");
-    e = launch_swap_stage(swkind, 2, q2, swap_row_bytes(swkind, 2) == 64 ? c->tm_w2sw : c->tm_w2tc, tm_inter,
-                          (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
+    e = launch_swap_stage(swkind, 2, use_packed, 1, q2,
+                          use_packed ? c->tm_w2pk : (swap_row_bytes(swkind, 2) == 64 ? c->tm_w2sw : c->tm_w2tc),
+                          tm_inter, (int)(u2 < c->num_sms ? u2 : c->num_sms), st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
 
-  if (!fold) {
-    prof_mark(c, st, "finalize");
-    e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
-    if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
-  }
+  prof_mark(c, st, "finalize");
+  e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
   prof_mark(c, st, "end");
   return MOE_OK;
 }
@@ -665,6 +700,41 @@ moe_status moe_read_profile(moe_ctx* c, float* ms, const char** names, int* coun
     if (names) names[i] = c->ev_name[i];
   }
   *count = n;
+  return MOE_OK;
+}
+
+moe_status moe_prepack_size(moe_ctx* c, int64_t* bytes) {
+  if (!c || !bytes) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  *bytes = (int64_t)c->E * c->H * (c->I / 2) + (int64_t)c->E * c->H * (c->I / 32);
+  return MOE_OK;
+}
+
+moe_status moe_prepack(moe_ctx* c, const uint8_t* w2, const uint8_t* w2s, int a_dtype, void* packed, void* stream) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
+  if (!packed) {  // unbind
+    c->pk_src = nullptr;
+    c->pk_codes = c->pk_scales = nullptr;
+    c->tm_w2pk_key = nullptr;
+    return MOE_OK;
+  }
+  if (!w2 || !w2s) return fail(MOE_ERR_INVALID_ARG, "NULL weight pointer");
+  if (a_dtype != MOE_A_BF16 && a_dtype != MOE_A_FP8 && a_dtype != MOE_A_FP4)
+    return fail(MOE_ERR_UNSUPPORTED, "a_dtype %d unknown", a_dtype);
+  if (!aligned16(w2) || !aligned16(w2s) || !aligned16(packed))
+    return fail(MOE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  CUDA_TRY(cudaSetDevice(c->device));
+  uint8_t* pc = static_cast<uint8_t*>(packed);
+  uint8_t* ps = pc + (size_t)c->E * c->H * (c->I / 2);
+  // kind::mxf4 (bf16 and fp4 activations) reads the blocks pre-swizzled by one bulk copy;
+  // kind::mxf8f6f4 (fp8) through the unpacking TMA, rows in order
+  cudaError_t e = launch_prepack_w2(w2, w2s, c->E, c->H, c->I, a_dtype != MOE_A_FP8, pc, ps, c->num_sms,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prepack launch");
+  c->pk_src = w2;
+  c->pk_adt = a_dtype;
+  c->pk_codes = pc;
+  c->pk_scales = ps;
+  c->tm_w2pk_key = nullptr;
   return MOE_OK;
 }
 

@@ -48,10 +48,9 @@ def gpu_f64(out):
     return out.float().cpu().numpy().astype(np.float64)
 
 
-E2M1_GRID = np.array(sorted(set(np.concatenate([-E2M1, E2M1]))))
-E4M3_GRID = np.array(sorted(set(torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
-                                 .numpy().tolist()) - {float("nan")}))
-E4M3_GRID = E4M3_GRID[np.isfinite(E4M3_GRID)]
+E2M1_GRID = np.unique(np.concatenate([-E2M1, E2M1]))
+_E4M3_ALL = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+E4M3_GRID = np.unique(_E4M3_ALL[np.isfinite(_E4M3_ALL)])  # sorted, -0 and +0 as one value
 
 
 def check_requant_rows(codes, scales, y32, a_dtype, tol=1e-3):

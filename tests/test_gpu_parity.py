@@ -373,18 +373,41 @@ def test_argument_errors_are_reported_before_launch():
     assert e.value.status == 1
 
 
-@pytest.mark.parametrize("switches", [{"MOE_FUSED": "1"}, {"MOE_FOLD": "1"}, {"MOE_EARLY": "0"},
-                                      {"MOE_FUSED": "1", "MOE_FOLD": "1"}])
-@pytest.mark.parametrize("a_dtype", ["bf16", "fp8"])
-def test_launch_sequence_switches(switches, a_dtype, monkeypatch):
-    """The alternative launch sequences (sort and scatter in one launch; the finalize
-    inside stage 2; no weight loads before the wait on the previous kernel) give the
-    oracle's results too."""
-    for k, v in switches.items():
-        monkeypatch.setenv(k, v)
-    for T, seed in ((1, 3), (24, 4)):
+@pytest.mark.parametrize("a_dtype", ["bf16", "fp8", "fp4"])
+def test_fused_sort_and_scatter(a_dtype, monkeypatch):
+    """The sort and the activation scatter in one launch (MOE_FUSED=1 at context
+    creation; every CTA sorts in shared memory, CTA 0 publishes) gives the oracle's
+    results and the same sort as the separate kernels."""
+    monkeypatch.setenv("MOE_FUSED", "1")
+    for T, seed in ((1, 3), (24, 4), (512, 5)):
         case = make_case(T, 3584, 384, 896, 16, "uniform", 123 + seed)
-        ctx = moe.MoE(3584, 384, 896, 16, 32)
+        ctx = moe.MoE(3584, 384, 896, 16, 512)
         out, _ = run_gpu(case, "situv2", a_dtype, ctx=ctx)
-        check_out(out, case, "situv2", a_dtype)
+        subset = None if T < 64 else np.array([0, 77, 511], np.int32)
+        check_out(out, case, "situv2", a_dtype, subset=subset)
+        srt = ctx.last_sort()
+        ref = oracle.sort(case["ids"].numpy(), 896, srt["tile_m"])
+        assert np.array_equal(srt["sorted_ids"].cpu().numpy(), ref["sorted_ids"])
+        assert np.array_equal(srt["expert_offset"].cpu().numpy(), ref["expert_offset"])
         assert ctx.get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("a_dtype", ["bf16", "fp8", "fp4"])
+def test_split_k_stage1(a_dtype, monkeypatch):
+    """At a few tokens the few-rows stage 1 splits K over clusters of 2-3 CTAs and
+    applies the activation after adding the partial sums (rank 0, through distributed
+    shared memory); the result matches the oracle and the unsplit kernel."""
+    # TP8 T=1: 48 units, clusters of 3; H=1024: 4 K tiles over 3 ranks; H=256: 2 fp8 K tiles over 2
+    for T, H, I, E, K in ((1, 3584, 384, 896, 16), (1, 1024, 256, 64, 4), (16, 256, 128, 8, 2)):
+        case = make_case(T, H, I, E, K, "uniform", 900 + T, experts_all=E <= 8)
+        outs = []
+        for split in ("1", "0"):
+            monkeypatch.setenv("MOE_SPLITK", split)
+            ctx = moe.MoE(H, I, E, K, T)
+            out, _ = run_gpu(case, "situv2", a_dtype, ctx=ctx)
+            check_out(out, case, "situv2", a_dtype)
+            if split == "1":
+                check_intermediate(ctx, case, "situv2", a_dtype)
+            assert ctx.get_error() == (0, 0)
+            outs.append(gpu_f64(out))
+        assert token_rel_l2(outs[0], outs[1]) <= (2e-3 if a_dtype == "bf16" else 2e-2)
