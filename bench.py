@@ -93,6 +93,26 @@ def max_over_ranks(pg, v, device):
     return float(t.item())
 
 
+def whole_job(pg, step_ms, world, device):
+    """Replicas: every rank runs the same calls on its own GPU, no collective on the
+    data path. Returns (the slowest rank's ms per step, us per call of the whole job =
+    that time over the calls all ranks made in it)."""
+    ms = max_over_ranks(pg, step_ms, device)
+    return ms, ms * 1000.0 / world
+
+
+def relaunch_as_replicas(n):
+    """`--gpus N` without a launcher: run N replicas of this command under torchrun (one
+    process per GPU, rendezvous on 127.0.0.1)."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=%d" % n,
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    os.execv(sys.executable, cmd)
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -318,9 +338,8 @@ def run_ours(args, world, rank, local, pg):
     sampler.stop()
     clocks = sampler.summary(t_soak, t2)
 
+    step_ms_max, value_us = whole_job(pg, statistics.mean(ms), world, device)
     step_ms = statistics.mean(ms)
-    step_ms_max = max_over_ranks(pg, step_ms, device)
-    value_us = step_ms_max * 1000.0 / world  # whole job: calls of all ranks over the slowest rank's time
 
     # --- per-kernel breakdown (separate, profiled pass)
     ctx.set_profiling(True)
@@ -559,7 +578,11 @@ def main():
     select_config(args.config)
     if args.tokens is None:
         args.tokens = HEAD_T
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        relaunch_as_replicas(args.gpus)
     world, rank, local, pg = dist_setup()
+    if world != args.gpus:
+        ap.error("--gpus %d but %d ranks were launched" % (args.gpus, world))
     if args.impl == "reference":
         res = run_reference(args, world, rank, local, pg)
     else:
