@@ -61,6 +61,9 @@ def lib():
         L.orc_requantize_intermediate.argtypes = [vp, i32, i32, vp]
         L.orc_expert_stage1.restype = i64
         L.orc_expert_stage1.argtypes = [vp, vp, i32, i32, i32, vp, vp, i32, d, d, i32, vp, vp]
+        L.orc_ep_forward.restype = i64
+        L.orc_ep_forward.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                     i32, d, d, i32, i32, vp, i32, vp, vp]
         L.orc_route.restype = i64
         L.orc_route.argtypes = [vp, i32, i32, i32, vp, vp]
         L.orc_num_threads.restype = i32
@@ -239,6 +242,33 @@ def expert_stage1(x_bits, tokens, w13e, w13se, act_kind, beta, lbeta, a_dtype):
     if st != 0:
         raise ValueError("oracle rejected the arguments")
     return y32, yq
+
+
+def ep_forward(x_bf16, ids, w, w13, w13s, w2, w2s, ranks, act_kind, beta, lbeta, a_dtype, wire=True,
+               subset=None):
+    """Expert-parallel oracle: `ranks` ranks own equal slices of the E experts; each
+    rank's share of a token goes over an fp8 1x32 combine wire (wire=True) and the
+    shares are summed. Returns (out_f64 [n,H], out_bf16 uint16 [n,H])."""
+    x_bf16 = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    T, H = x_bf16.shape
+    K = ids.shape[1]
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    assert E % ranks == 0
+    sub = None if subset is None else _c(subset, np.int32)
+    n = T if sub is None else sub.size
+    out_f64 = np.zeros((n, H), dtype=np.float64)
+    out_bf16 = np.zeros((n, H), dtype=np.uint16)
+    st = lib().orc_ep_forward(
+        _p(x_bf16), _p(ids), _p(w), T, H, I, E // ranks, ranks, K,
+        _p(_c(w13, np.uint8)), _p(_c(w13s, np.uint8)), _p(_c(w2, np.uint8)), _p(_c(w2s, np.uint8)),
+        ACT[act_kind], float(beta), float(lbeta), ADTYPE[a_dtype], 1 if wire else 0, _p(sub), n,
+        _p(out_f64), _p(out_bf16))
+    if st != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out_f64, out_bf16
 
 
 def route(logits, K):

@@ -478,6 +478,61 @@ int64_t orc_moe_dense(const uint16_t* x, const int32_t* ids, const float* w,
     return dropped;
 }
 
+/* ---------------------------------------------------------------------------
+ * Expert parallelism over R ranks ("Add Kimi-K3 A8W4 support to the FlyDSL
+ * MegaMoE V2 operator", Motivation and Technical Details: EP8 with 112 experts
+ * per rank; each rank computes its experts' share of a token and sends it back
+ * over the combine wire, quantised to fp8 blockwise 1x32). Rank r owns global
+ * experts [r*El, (r+1)*El). Its share of token t is the top-k-weighted sum of
+ * the stage-2 rows of t's pairs routed to it (the grouped forward with every
+ * other pair dropped), held in fp32; with wire != 0 it is then quantised to
+ * e4m3 with 1x32 e8m0 scales along H and dequantised (the wire), and the
+ * shares are added over r (fp64) and rounded once to bf16.
+ * ------------------------------------------------------------------------- */
+int64_t orc_ep_forward(const uint16_t* x, const int32_t* ids, const float* w,
+                       int T, int H, int I, int El, int R, int K,
+                       const uint8_t* w13, const uint8_t* w13s,
+                       const uint8_t* w2, const uint8_t* w2s,
+                       int act, double beta, double lbeta, int a_dtype, int wire,
+                       const int32_t* subset, int nsub,
+                       double* out_f64, uint16_t* out_bf16) {
+    if (bad_shape(T, H, I, El, K) || R <= 0) return -1;
+    if (!subset) nsub = T;
+    int64_t n = (int64_t)T * K;
+    int32_t* ids_r = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    double* part = (double*)malloc(sizeof(double) * (size_t)nsub * H + 1);
+    double* p32 = (double*)malloc(sizeof(double) * (size_t)H);
+    double* deq = (double*)malloc(sizeof(double) * (size_t)H);
+    uint8_t* codes = (uint8_t*)malloc((size_t)H);
+    uint8_t* scales = (uint8_t*)malloc((size_t)(H / 32));
+    for (int64_t i = 0; i < (int64_t)nsub * H; ++i) out_f64[i] = 0.0;
+    for (int r = 0; r < R; ++r) {
+        for (int64_t p = 0; p < n; ++p)
+            ids_r[p] = (ids[p] >= r * El && ids[p] < (r + 1) * El) ? ids[p] - r * El : -1;
+        const size_t e0 = (size_t)r * El;
+        int64_t st = orc_moe_forward(x, ids_r, w, T, H, I, El, K,
+                                     w13 + e0 * 2 * I * (H / 2), w13s + e0 * 2 * I * (H / 32),
+                                     w2 + e0 * H * (I / 2), w2s + e0 * H * (I / 32),
+                                     act, beta, lbeta, a_dtype, 16, subset, nsub, part, NULL, NULL);
+        if (st < 0) { nsub = -1; break; }
+        for (int i = 0; i < nsub; ++i) {
+            const double* pr = part + (size_t)i * H;
+            if (wire) {
+                for (int h = 0; h < H; ++h) p32[h] = (double)(float)pr[h];  /* the share is held in fp32 */
+                orc_mx_quantize_f64(p32, H / 32, ORC_FMT_E4M3, codes, scales);
+                orc_mx_dequantize(codes, scales, H / 32, ORC_FMT_E4M3, deq);
+                for (int h = 0; h < H; ++h) out_f64[(size_t)i * H + h] += deq[h];
+            } else {
+                for (int h = 0; h < H; ++h) out_f64[(size_t)i * H + h] += pr[h];
+            }
+        }
+    }
+    if (nsub >= 0 && out_bf16)
+        for (int64_t i = 0; i < (int64_t)nsub * H; ++i) out_bf16[i] = orc_bf16_from_f64(out_f64[i]);
+    free(ids_r); free(part); free(p32); free(deq); free(codes); free(scales);
+    return nsub < 0 ? -1 : 0;
+}
+
 /* Stage 1 of one expert for a list of token rows (the same steps as the grouped
  * forward: activation operand, g and u against the expert's dequantised gate and
  * up rows, act, fp32 holding, requantisation). */

@@ -100,6 +100,20 @@ int64_t orc_expert_stage1(const uint16_t* x, const int32_t* tokens, int nrows, i
                           const uint8_t* w13e, const uint8_t* w13se, int act, double beta, double lbeta,
                           int a_dtype, double* y32, double* yq);
 
+/* Expert parallelism over R ranks of El experts each (global ids [0, R*El)):
+ * rank r's share of every token (its routed pairs' weighted stage-2 rows, the
+ * grouped forward with the other pairs dropped) held in fp32, with wire != 0
+ * quantised to e4m3 1x32 (e8m0 scales along H) and dequantised, then summed
+ * over the ranks and rounded once to bf16. Weights are the global arrays.
+ * Arguments otherwise as orc_moe_forward. Returns 0, or -1 on a bad argument. */
+int64_t orc_ep_forward(const uint16_t* x, const int32_t* ids, const float* w,
+                       int T, int H, int I, int El, int R, int K,
+                       const uint8_t* w13, const uint8_t* w13s,
+                       const uint8_t* w2, const uint8_t* w2s,
+                       int act, double beta, double lbeta, int a_dtype, int wire,
+                       const int32_t* subset, int nsub,
+                       double* out_f64, uint16_t* out_bf16);
+
 /* Top-k softmax router over E logits per token (fp32 [T,E], finite or -inf,
  * at least one finite per token): ids [T,K] in descending logit order (equal
  * logits: lower id first), weights [T,K] = the softmax probabilities of those
