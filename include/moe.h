@@ -262,6 +262,37 @@ moe_status moe_set_profiling(moe_ctx* ctx, int enable);
  * *count is the capacity on entry and the number written on return. */
 moe_status moe_read_profile(moe_ctx* ctx, float* ms, const char** names, int* count);
 
+/* Expert parallelism emulated on one GPU ("Add Kimi-K3 A8W4 support to the
+ * FlyDSL MegaMoE V2 operator": EP8 with 112 experts per rank; tokens dispatched
+ * to the ranks owning their experts; each rank's stage-2 result sent back over
+ * the combine wire quantised to fp8 blockwise 1x32). `ranks` ranks (<= 16) own
+ * equal slices of the global experts: rank r owns [r*El, (r+1)*El), where El =
+ * experts_per_rank. moe_ep_forward takes the same arguments as moe_forward, with
+ * global expert ids and the global weight arrays [ranks*El, ...], and runs:
+ *   dispatch: for each rank, the tokens with a pair routed to it (token order)
+ *     copied into the rank's receive buffer (bf16 x, local ids with -1 for the
+ *     pairs of other ranks, top-k weights) -- then one stream synchronisation so
+ *     that the host knows each rank's token count (moe_ep_counts);
+ *   per rank: the forward pass on its received tokens against its slice of the
+ *     weights, its fp32 share of each token kept (no bf16 rounding);
+ *   combine: each share quantised to e4m3 with an e8m0 scale per 32 along H
+ *     (the MX rule), dequantised and summed over ranks in rank order (fp32),
+ *     rounded once to bf16 into out (tokens without routed pairs get zeros).
+ * Ids outside [0, ranks*El) are dropped and flagged (moe_ep_get_error). All
+ * buffers are allocated at moe_ep_create for max_tokens tokens per call. */
+typedef struct moe_ep moe_ep;
+moe_status moe_ep_create(moe_ep** ep, int hidden, int inter, int experts_per_rank, int ranks, int topk,
+                         int max_tokens, int device);
+moe_status moe_ep_destroy(moe_ep* ep);
+moe_status moe_ep_forward(moe_ep* ep, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                          int num_tokens, const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
+                          const uint8_t* w2_scale, int act, float beta, float linear_beta, int a_dtype, void* out,
+                          void* stream);
+/* Tokens each rank received in the last moe_ep_forward (host int32 [ranks]). */
+moe_status moe_ep_counts(moe_ep* ep, int32_t* counts);
+/* moe_get_error over the ranks: the union of their device flags, the first non-OK status. */
+moe_status moe_ep_get_error(moe_ep* ep, int32_t* device_flags);
+
 /* Prepacked stage-2 weights (an optimisation of the few-rows path; the plain
  * layout stays the contract and is still needed by the many-rows path).
  * moe_prepack_size: bytes of the packed copy (as many as w2 + w2_scale).

@@ -66,6 +66,11 @@ def lib():
         L.moe_quantize_mxfp4.argtypes = [vp, i64, i32, vp, vp, vp]
         L.moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.moe_selftest_wait.argtypes = [vp, i64, i32, vp]
+        L.moe_ep_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, i32]
+        L.moe_ep_destroy.argtypes = [vp]
+        L.moe_ep_forward.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, f32, f32, i32, vp, vp]
+        L.moe_ep_counts.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_ep_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         L.moe_prepack_size.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
         L.moe_prepack.argtypes = [vp, vp, vp, i32, vp, vp]
         L.moe_debug_inject.argtypes = [i32, i64]
@@ -80,7 +85,8 @@ def lib():
         L.moe_last_error_message.argtypes = []
         for name in ("moe_create", "moe_destroy", "moe_sort", "moe_forward", "moe_forward_host",
                      "moe_quantize_activations", "moe_quantize_mxfp4", "moe_route", "moe_get_workspace",
-                     "moe_selftest_wait", "moe_debug_inject", "moe_prepack_size", "moe_prepack", "moe_get_error",
+                     "moe_selftest_wait", "moe_debug_inject", "moe_prepack_size", "moe_prepack",
+                     "moe_ep_create", "moe_ep_destroy", "moe_ep_forward", "moe_ep_counts", "moe_ep_get_error", "moe_get_error",
                      "moe_set_profiling", "moe_read_profile"):
             getattr(L, name).restype = i32
         _lib = L
@@ -298,6 +304,53 @@ def quantize_activations(x, a_dtype, stream=None):
     _check(lib().moe_quantize_activations(_ptr(x), T, H, ADTYPE[a_dtype], _ptr(codes), _ptr(scales),
                                           _stream(stream)))
     return codes, scales
+
+
+class MoEEP:
+    """Expert parallelism emulated on one GPU: `ranks` ranks of experts_per_rank experts,
+    dispatch to receive buffers, per-rank forward, fp8 1x32 combine wire (moe_ep_*)."""
+
+    def __init__(self, hidden, inter, experts_per_rank, ranks, topk, max_tokens, device=0):
+        self.H, self.R = hidden, ranks
+        h = ctypes.c_void_p()
+        _check(lib().moe_ep_create(ctypes.byref(h), hidden, inter, experts_per_rank, ranks, topk, max_tokens, device))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().moe_ep_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, act="situv2", beta=4.0,
+                linear_beta=25.0, a_dtype="bf16", out=None, stream=None):
+        _require(x, torch.bfloat16, "x")
+        _require(topk_ids, torch.int32, "topk_ids")
+        _require(topk_weights, torch.float32, "topk_weights")
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
+        _check(lib().moe_ep_forward(self._h, _ptr(x), _ptr(topk_ids), _ptr(topk_weights), T, _ptr(w13),
+                                    _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), ACT[act], float(beta),
+                                    float(linear_beta), ADTYPE[a_dtype], _ptr(out), _stream(stream)))
+        return out
+
+    def counts(self):
+        c = (ctypes.c_int32 * self.R)()
+        _check(lib().moe_ep_counts(self._h, c))
+        return list(c)
+
+    def get_error(self):
+        f = ctypes.c_int32(0)
+        st = lib().moe_ep_get_error(self._h, ctypes.byref(f))
+        if st not in (0, 5, 6):
+            _check(st)
+        return st, f.value
 
 
 def debug_inject_alloc_failure(n):

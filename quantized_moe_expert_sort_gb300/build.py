@@ -10,7 +10,7 @@ BUILD = os.path.join(HERE, "_build")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
 SOURCES = ["moe_api.cu", "kernels_prep.cu", "kernels_tc.cu", "kernels_swap.cu", "kernels_route.cu",
-           "kernels_pack.cu", "sort_noalloc.cu"]
+           "kernels_pack.cu", "kernels_ep.cu", "sort_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

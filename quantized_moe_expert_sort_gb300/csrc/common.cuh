@@ -137,8 +137,35 @@ __device__ __forceinline__ float act_apply(int act, float g, float u, float beta
 }
 
 // ---------------------------------------------------------------------------
-// Warp helpers
+// Warp and block helpers
 // ---------------------------------------------------------------------------
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* smem32, int* total) {
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem32[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? smem32[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem32[lane] = w;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  int before = (warp > 0 ? smem32[warp - 1] : 0) + x - v;
+  *total = smem32[nw - 1];
+  __syncthreads();
+  return before;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));

@@ -21,6 +21,7 @@ struct SortOut {
   int32_t* meta;            // [META_WORDS] num_blocks, num_active, num_rows
   int32_t* pair_row = nullptr;  // [T*K] (optional) sorted row of each pair, -1 if dropped
   int4* active_info = nullptr;  // [E]   (optional) {expert, count, first row, 0} of each active expert
+  int neg_masked = 0;           // 1: negative ids mean "no expert here" (skipped, not flagged)
 };
 
 constexpr int SORT_SMALL_MAX_PAIRS = 8192;  // single-CTA sort up to this many pairs
@@ -96,6 +97,17 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int complete, int* err, cuda
 // [E][H/128][I/128] (byte 16*(r%32) + 4*(r/32) + b for row r, 32-block b).
 cudaError_t launch_prepack_w2(const uint8_t* w2, const uint8_t* w2s, int E, int H, int I, int swz, uint8_t* pc,
                               uint8_t* ps, int num_sms, cudaStream_t st);
+
+// Expert-parallel emulation (kernels_ep.cu): ranks of El experts, received rows [R][maxT].
+constexpr int EP_MAX_RANKS = 16;
+struct EpShares {
+  const float* acc[EP_MAX_RANKS];  // each rank's fp32 share [its received rows, H]
+};
+cudaError_t launch_ep_dispatch(const void* x, const int32_t* ids, const float* w, int T, int H, int K, int El, int R,
+                               int maxT, int32_t* recv_tok, int32_t* recv_ids, float* recv_w, int32_t* slot,
+                               int32_t* counts, void* recv_x, int* err, int num_sms, cudaStream_t st);
+cudaError_t launch_ep_combine(const EpShares& shares, const int32_t* counts, const int32_t* slot, int T, int H, int R,
+                              int maxT, uint8_t* codes, uint8_t* scales, void* out, int num_sms, cudaStream_t st);
 
 // Top-k softmax router over E logits per token (kernels_route.cu).
 constexpr int ROUTE_MAX_EXPERTS = 4096;

@@ -17,33 +17,6 @@ namespace moe {
 // Sort building blocks
 // ---------------------------------------------------------------------------
 
-// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* smem32, int* total) {
-  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) smem32[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? smem32[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-      if (lane >= o) w += y;
-    }
-    smem32[lane] = w;  // inclusive prefix of warp sums
-  }
-  __syncthreads();
-  int before = (warp > 0 ? smem32[warp - 1] : 0) + x - v;
-  *total = smem32[nw - 1];
-  __syncthreads();
-  return before;
-}
-
 // Scan of padded per-expert counts: writes expert_count, expert_offset,
 // active list, meta, block_expert and the padding sentinels.
 // cnt[e] (shared) holds counts on entry; on exit cursor[e] = expert_offset[e].
@@ -170,7 +143,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t* __restr
   for (int p = threadIdx.x; p < n; p += blockDim.x) {
     int e = ids[p];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else bad = true;
+    else if (!(so.neg_masked && e < 0)) bad = true;
   }
   if (bad) set_error(err, DEV_ERR_BAD_EXPERT);
   __syncthreads();
@@ -181,7 +154,7 @@ __global__ void __launch_bounds__(1024) sort_small_kernel(const int32_t* __restr
 
 // Multi-CTA sort, pass 1: per-chunk histograms hist[g][e].
 __global__ void __launch_bounds__(1024) sort_hist_kernel(const int32_t* __restrict__ ids, long n, int E, int chunk,
-                                                         int* __restrict__ hist, int* err) {
+                                                         int* __restrict__ hist, int* err, int neg_masked) {
   extern __shared__ __align__(16) uint8_t smem[];
   int* cnt = reinterpret_cast<int*>(smem);
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
@@ -191,7 +164,7 @@ __global__ void __launch_bounds__(1024) sort_hist_kernel(const int32_t* __restri
   for (long p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
     int e = ids[p];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else bad = true;
+    else if (!(neg_masked && e < 0)) bad = true;
   }
   if (bad) set_error(err, DEV_ERR_BAD_EXPERT);
   __syncthreads();
@@ -520,7 +493,7 @@ __global__ void __launch_bounds__(1024) sort_scatter_kernel(const int32_t* __res
   for (int p = threadIdx.x; p < n; p += blockDim.x) {
     int e = ids[p];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else bad = true;
+    else if (!(so.neg_masked && e < 0)) bad = true;
   }
   if (bad && lead) set_error(err, DEV_ERR_BAD_EXPERT);
   __syncthreads();
@@ -605,7 +578,7 @@ cudaError_t launch_sort(const int32_t* ids, long n, int E, int tile_m, const Sor
   int chunk = SORT_CHUNK;
   int G = (int)((n + chunk - 1) / chunk);
   if (G > hist_cap_chunks) return cudaErrorInvalidValue;
-  sort_hist_kernel<<<G, 1024, (size_t)E * 4, st>>>(ids, n, E, chunk, hist, err);
+  sort_hist_kernel<<<G, 1024, (size_t)E * 4, st>>>(ids, n, E, chunk, hist, err, so.neg_masked);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess)
     e = launch_k(sort_scan_kernel, dim3(1), dim3(1024), (size_t)E * 8 + 32 * 4, st, true, hist, G, E, tile_m, (int)n, so);

@@ -411,9 +411,14 @@ moe_status moe_sort(moe_ctx* c, const int32_t* ids, int T, int tile_m, moe_sort_
   return MOE_OK;
 }
 
-moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const float* w, int T, const uint8_t* w13,
-                       const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act, float beta,
-                       float lbeta, int adt, void* out, void* stream) {
+}  // extern "C"
+
+// The forward pass behind moe_forward. out == nullptr: no finalize, the fp32 sums
+// stay in c->acc32 (the expert-parallel emulation reads them); neg_masked: negative
+// expert ids mean "no expert here" (skipped, not flagged).
+static moe_status forward_impl(moe_ctx* c, const void* x, const int32_t* ids, const float* w, int T,
+                               const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act,
+                               float beta, float lbeta, int adt, void* out, void* stream, bool neg_masked) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "ctx is NULL");
   if (T < 0 || T > c->max_tokens) return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", T, c->max_tokens);
   if (act != MOE_ACT_SILU && act != MOE_ACT_SITUV2) return fail(MOE_ERR_UNSUPPORTED, "activation %d is not silu or situv2", act);
@@ -421,7 +426,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   if (act == MOE_ACT_SITUV2 && !(beta > 0.0f && lbeta > 0.0f && beta < 3e38f && lbeta < 3e38f))
     return fail(MOE_ERR_INVALID_ARG, "SiTUv2 needs finite beta > 0 and linear_beta > 0");
   if (T == 0) return MOE_OK;
-  const void* ptrs[] = {x, ids, w, w13, w13s, w2, w2s, out};
+  const void* ptrs[] = {x, ids, w, w13, w13s, w2, w2s, out ? out : x};
   for (const void* p : ptrs) {
     if (!p) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -493,6 +498,7 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
   c->ev_n = 0;
   SortOut so = sort_out(c);
   so.pair_row = c->pair_row;
+  so.neg_masked = neg_masked ? 1 : 0;
   if (use_sw) so.active_info = c->active_info;
   c->last_tile_m = tile_m;
   c->last_inter_layout = use_tc ? 1 : (adt == MOE_A_BF16 ? 2 : 0);
@@ -605,11 +611,155 @@ moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const floa
     if (e != cudaSuccess) return cuda_fail(e, "stage-2 launch");
   }
 
-  prof_mark(c, st, "finalize");
-  e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
-  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  if (out) {
+    prof_mark(c, st, "finalize");
+    e = launch_finalize(c->acc32, (long)T * c->H, out, c->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  }
   prof_mark(c, st, "end");
   return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Expert-parallel emulation (kernels_ep.cu)
+// ---------------------------------------------------------------------------
+struct moe_ep {
+  int H, I, El, R, K, max_tokens, device, num_sms;
+  moe_ctx* rank[EP_MAX_RANKS];
+  void* recv_x;        // [R][max_tokens][H] bf16: the dispatch payload
+  int32_t* recv_tok;   // [R][max_tokens]
+  int32_t* recv_ids;   // [R][max_tokens][K] local expert ids, -1 for the pairs of other ranks
+  float* recv_w;       // [R][max_tokens][K]
+  int32_t* slot;       // [max_tokens][R] row of each token on each rank, -1 if not sent there
+  int32_t* counts;     // [R] received tokens per rank (device)
+  int32_t* counts_h;   // [R] (pinned host)
+  uint8_t* wire_q;     // [R][max_tokens][H] e4m3: the combine payload
+  uint8_t* wire_s;     // [R][max_tokens][H/32] e8m0
+};
+
+static void free_ep(moe_ep* p) {
+  for (int r = 0; r < EP_MAX_RANKS; ++r)
+    if (p->rank[r]) moe_destroy(p->rank[r]);
+  void* ptrs[] = {p->recv_x, p->recv_tok, p->recv_ids, p->recv_w, p->slot, p->counts, p->wire_q, p->wire_s};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+  if (p->counts_h) cudaFreeHost(p->counts_h);
+  delete p;
+}
+
+extern "C" {
+
+moe_status moe_ep_create(moe_ep** out, int H, int I, int El, int R, int K, int max_tokens, int device) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out-pointer is NULL");
+  *out = nullptr;
+  if (R < 1 || R > EP_MAX_RANKS) return fail(MOE_ERR_UNSUPPORTED, "ranks must be in [1, %d]", EP_MAX_RANKS);
+  moe_ep* p = new moe_ep();
+  std::memset(p, 0, sizeof(*p));
+  p->H = H; p->I = I; p->El = El; p->R = R; p->K = K; p->max_tokens = max_tokens; p->device = device;
+  for (int r = 0; r < R; ++r) {
+    moe_status s = moe_create(&p->rank[r], H, I, El, K, max_tokens, device);
+    if (s != MOE_OK) {
+      free_ep(p);
+      return s;
+    }
+  }
+  p->num_sms = p->rank[0]->num_sms;
+  const size_t rows = (size_t)R * max_tokens;
+  struct { void** q; size_t bytes; } allocs[] = {
+      {&p->recv_x, rows * H * 2},       {(void**)&p->recv_tok, rows * 4},     {(void**)&p->recv_ids, rows * K * 4},
+      {(void**)&p->recv_w, rows * K * 4}, {(void**)&p->slot, rows * 4},       {(void**)&p->counts, (size_t)R * 4},
+      {(void**)&p->wire_q, rows * H},   {(void**)&p->wire_s, rows * (H / 32)},
+  };
+  for (auto& a : allocs) {
+    cudaError_t e = cudaMalloc(a.q, a.bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      free_ep(p);
+      return fail(MOE_ERR_OOM, "cudaMalloc(%zu) failed: %s", a.bytes, cudaGetErrorString(e));
+    }
+  }
+  cudaError_t e = cudaMallocHost((void**)&p->counts_h, sizeof(int32_t) * R);
+  if (e != cudaSuccess) {
+    free_ep(p);
+    return cuda_fail(e, "cudaMallocHost");
+  }
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_ep_destroy(moe_ep* p) {
+  if (!p) return MOE_OK;
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  free_ep(p);
+  return MOE_OK;
+}
+
+moe_status moe_ep_forward(moe_ep* p, const void* x, const int32_t* ids, const float* w, int T, const uint8_t* w13,
+                          const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act, float beta, float lbeta,
+                          int adt, void* out, void* stream) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "ep is NULL");
+  if (T < 0 || T > p->max_tokens) return fail(MOE_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", T, p->max_tokens);
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, ids, w, w13, w13s, w2, w2s, out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return fail(MOE_ERR_INVALID_ARG, "NULL or misaligned tensor pointer");
+  CUDA_TRY(cudaSetDevice(p->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int H = p->H, I = p->I, El = p->El, R = p->R, K = p->K, M = p->max_tokens;
+  // dispatch: each rank's received rows, then the counts to the host (one sync)
+  cudaError_t e = launch_ep_dispatch(x, ids, w, T, H, K, El, R, M, p->recv_tok, p->recv_ids, p->recv_w, p->slot,
+                                     p->counts, p->recv_x, p->rank[0]->err, p->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  CUDA_TRY(cudaMemcpyAsync(p->counts_h, p->counts, sizeof(int32_t) * R, cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(cudaStreamSynchronize(st));
+  // each rank: its received rows against its slice of the experts, fp32 shares kept
+  EpShares sh{};
+  for (int r = 0; r < R; ++r) {
+    const size_t e0 = (size_t)r * El;
+    const uint8_t* rw13 = w13 + e0 * 2 * I * (H / 2);
+    const uint8_t* rw13s = w13s + e0 * 2 * I * (H / 32);
+    const uint8_t* rw2 = w2 + e0 * H * (I / 2);
+    const uint8_t* rw2s = w2s + e0 * H * (I / 32);
+    const int Tr = p->counts_h[r];
+    sh.acc[r] = p->rank[r]->acc32;
+    if (Tr == 0) continue;
+    moe_status s = forward_impl(p->rank[r], static_cast<const uint8_t*>(p->recv_x) + (size_t)r * M * H * 2,
+                                p->recv_ids + (size_t)r * M * K, p->recv_w + (size_t)r * M * K, Tr, rw13, rw13s, rw2,
+                                rw2s, act, beta, lbeta, adt, nullptr, stream, true);
+    if (s != MOE_OK) return s;
+  }
+  // combine: each rank's shares over the fp8 1x32 wire, summed per token
+  e = launch_ep_combine(sh, p->counts, p->slot, T, H, R, M, p->wire_q, p->wire_s, out, p->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return MOE_OK;
+}
+
+moe_status moe_ep_counts(moe_ep* p, int32_t* counts) {
+  if (!p || !counts) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  for (int r = 0; r < p->R; ++r) counts[r] = p->counts_h[r];
+  return MOE_OK;
+}
+
+moe_status moe_ep_get_error(moe_ep* p, int32_t* flags) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "ep is NULL");
+  int32_t all = 0;
+  moe_status worst = MOE_OK;
+  for (int r = 0; r < p->R; ++r) {
+    int32_t f = 0;
+    moe_status s = moe_get_error(p->rank[r], &f);
+    all |= f;
+    if (s != MOE_OK && worst == MOE_OK) worst = s;
+  }
+  if (flags) *flags = all;
+  return worst;
+}
+
+moe_status moe_forward(moe_ctx* c, const void* x, const int32_t* ids, const float* w, int T, const uint8_t* w13,
+                       const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int act, float beta,
+                       float lbeta, int adt, void* out, void* stream) {
+  if (T > 0 && !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+  return forward_impl(c, x, ids, w, T, w13, w13s, w2, w2s, act, beta, lbeta, adt, out, stream, false);
 }
 
 moe_status moe_forward_host(moe_ctx* c, const void* x_host, const int32_t* ids_host, const float* w_host, int T,
