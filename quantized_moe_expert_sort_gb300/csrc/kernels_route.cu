@@ -11,10 +11,19 @@
 // the chosen K alone (the full-softmax denominator cancels):
 //   w_k = exp(l_k - l_max) / sum_j exp(l_j - l_max),  j over the K chosen.
 //
-// One warp per token: the logits row is staged in shared memory; lane l owns
-// elements l, l + 32, ...; each round the warp takes the maximum of the lanes'
-// current best (value, then lowest id) with two hardware reductions, the owner
-// lane marks it taken and rescans its own elements.
+// One warp per token; the logits row is staged in shared memory, lane l owning
+// elements l, l + 32, ....  Selection is exact in two steps:
+//  1. Threshold. With t0 the K-th largest of the 32 lanes' maxima, at least K
+//     elements are >= t0 (those K maxima), so the K-th largest logit is >= t0
+//     and every element of the top K -- ties at the boundary included -- is
+//     among the candidates {e : l_e >= t0}.  For Gaussian logits (E = 896,
+//     K = 16) there are about 30 of them.
+//  2. Rank. Each candidate's output slot is the number of candidates before it
+//     in (logit descending, id ascending) order; slots below K are the result.
+// When more than kCandMax elements pass the threshold (heavy ties, e.g. a
+// quantised logit grid), the warp falls back to K rounds of "take the largest
+// remaining": the maximum of the lanes' current best (value, then lowest id)
+// with two hardware reductions, the owner lane marking it and rescanning.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,6 +31,14 @@ namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
+constexpr int kCandMax = 128;  // candidates above the threshold the rank step takes
+
+struct RouteScratch {  // per warp, after the staged logits rows
+  uint32_t ckey[kCandMax];
+  int32_t cid[kCandMax];
+  uint32_t skey[ROUTE_MAX_TOPK];
+  int32_t sid[ROUTE_MAX_TOPK];
+};
 
 // fp32 -> unsigned key with the same order (non-NaN inputs); -0 and +0 are
 // one key, as they compare equal.
@@ -42,38 +59,88 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const floa
   extern __shared__ __align__(16) float rsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* row = rsm + (size_t)warp * E;
-  const int per = (E + 31) / 32;  // elements per lane (<= MOE_ROUTE_MAX_EXPERTS / 32)
+  RouteScratch* rs = reinterpret_cast<RouteScratch*>(rsm + (size_t)kRouteWarps * E) + warp;
+  const int per = (E + 31) / 32;  // elements per lane (<= ROUTE_MAX_EXPERTS / 32)
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
   for (long t = (long)blockIdx.x * kRouteWarps + warp; t < T; t += (long)gridDim.x * kRouteWarps) {
     const float* src = logits + t * E;
-    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+    if (vec) {
+      for (int q = lane; q < E / 4; q += 32)
+        reinterpret_cast<float4*>(row)[q] = __ldg(reinterpret_cast<const float4*>(src) + q);
+    } else {
+      for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+    }
     __syncwarp();
-    uint32_t taken[4] = {0u, 0u, 0u, 0u};  // bit j: element lane + 32 j already chosen
-    auto rescan = [&](uint32_t* key, int* idx) {
-      uint32_t bk = 0u;
-      int bi = 0x7FFFFFFF;
-      for (int j = 0; j < per; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken[j >> 5] >> (j & 31)) & 1u)) {
-          const uint32_t k = order_key(row[e]);
-          if (bi == 0x7FFFFFFF || k > bk) { bk = k; bi = e; }  // strict: the lower id keeps ties
-        }
-      }
-      *key = bk;
-      *idx = bi;
-    };
-    uint32_t bk;
-    int bi;
-    rescan(&bk, &bi);
+    // 1. threshold: the K-th largest lane maximum (lanes without elements hold
+    // key 0, below every non-NaN logit's key; K <= E keeps them out of the top K)
+    uint32_t lm = 0u;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) lm = max(lm, order_key(row[e]));
+    }
+    int lr = 0;  // this lane's maximum ranked among the 32 (key descending, lane ascending)
+#pragma unroll 8
+    for (int l = 0; l < 32; ++l) {
+      const uint32_t o = __shfl_sync(0xFFFFFFFFu, lm, l);
+      lr += (o > lm) || (o == lm && l < lane);
+    }
+    const uint32_t t0 = __reduce_min_sync(0xFFFFFFFFu, lr < K ? lm : 0xFFFFFFFFu);
+    int C = 0;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane + 32 * j;
+      const uint32_t k = e < E ? order_key(row[e]) : 0u;
+      const bool pass = e < E && k >= t0;
+      const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
+      const int pos = C + __popc(b & lt_mask);
+      if (pass && pos < kCandMax) { rs->ckey[pos] = k; rs->cid[pos] = e; }
+      C += __popc(b);
+    }
+    __syncwarp();
     uint32_t my_key = 0u;
     int my_id = 0;
-    for (int k = 0; k < K; ++k) {
-      const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bi == 0x7FFFFFFF ? 0u : bk);
-      const int win = (int)__reduce_min_sync(0xFFFFFFFFu, (bi != 0x7FFFFFFF && bk == kmax) ? (uint32_t)bi : 0x7FFFFFFFu);
-      if (lane == k) { my_key = kmax; my_id = win; }
-      if ((win & 31) == lane) {  // the owner marks it and finds its next best
-        const int j = win >> 5;
-        taken[j >> 5] |= 1u << (j & 31);
-        rescan(&bk, &bi);
+    if (C <= kCandMax) {
+      // 2. rank the candidates; slot < K is the output position
+      for (int c = lane; c < C; c += 32) {
+        const uint32_t k = rs->ckey[c];
+        const int id = rs->cid[c];
+        int r = 0;
+        for (int d = 0; d < C; ++d) {
+          const uint32_t kd = rs->ckey[d];
+          r += (kd > k) || (kd == k && rs->cid[d] < id);
+        }
+        if (r < K) { rs->skey[r] = k; rs->sid[r] = id; }
+      }
+      __syncwarp();
+      if (lane < K) { my_key = rs->skey[lane]; my_id = rs->sid[lane]; }
+    } else {
+      uint32_t taken[4] = {0u, 0u, 0u, 0u};  // bit j: element lane + 32 j already chosen
+      auto rescan = [&](uint32_t* key, int* idx) {
+        uint32_t bk = 0u;
+        int bi = 0x7FFFFFFF;
+        for (int j = 0; j < per; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && !((taken[j >> 5] >> (j & 31)) & 1u)) {
+            const uint32_t k = order_key(row[e]);
+            if (bi == 0x7FFFFFFF || k > bk) { bk = k; bi = e; }  // strict: the lower id keeps ties
+          }
+        }
+        *key = bk;
+        *idx = bi;
+      };
+      uint32_t bk;
+      int bi;
+      rescan(&bk, &bi);
+      for (int k = 0; k < K; ++k) {
+        const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bi == 0x7FFFFFFF ? 0u : bk);
+        const int win =
+            (int)__reduce_min_sync(0xFFFFFFFFu, (bi != 0x7FFFFFFF && bk == kmax) ? (uint32_t)bi : 0x7FFFFFFFu);
+        if (lane == k) { my_key = kmax; my_id = win; }
+        if ((win & 31) == lane) {  // the owner marks it and finds its next best
+          const int j = win >> 5;
+          taken[j >> 5] |= 1u << (j & 31);
+          rescan(&bk, &bi);
+        }
       }
     }
     const float lmax = key_value(__shfl_sync(0xFFFFFFFFu, my_key, 0));
@@ -90,9 +157,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const floa
   }
 }
 
+static size_t route_smem_bytes(int E) { return sizeof(float) * kRouteWarps * E + sizeof(RouteScratch) * kRouteWarps; }
+
 cudaError_t route_set_smem_limits() {
   return cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(sizeof(float) * kRouteWarps * ROUTE_MAX_EXPERTS));
+                              (int)route_smem_bytes(ROUTE_MAX_EXPERTS));
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, int num_sms,
@@ -101,8 +170,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids,
   const long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  route_topk_kernel<<<(unsigned)blocks, kRouteWarps * 32, sizeof(float) * kRouteWarps * E, st>>>(logits, T, E, K, ids,
-                                                                                               weights);
+  route_topk_kernel<<<(unsigned)blocks, kRouteWarps * 32, route_smem_bytes(E), st>>>(logits, T, E, K, ids, weights);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,23 @@ def test_router_ids_bit_exact(T, E, K, grid):
     assert np.max(np.abs(w - rw)) <= 2e-6
 
 
+def test_router_all_equal_and_candidate_overflow():
+    # all logits equal: every element passes the lane-maximum threshold, so the
+    # exact fallback selection runs; ids are 0..K-1, weights 1/K
+    ids, w = _route(torch.full((5, 896), 0.5), 16)
+    assert np.array_equal(ids, np.tile(np.arange(16, dtype=np.int32), (5, 1)))
+    assert np.max(np.abs(w - 1.0 / 16)) <= 2e-6
+    # one block of 200 equal logits on top of noise: more candidates than the
+    # rank step takes on some rows, few on others
+    g = torch.Generator().manual_seed(7)
+    logits = torch.randn(257, 4096, generator=g) * 0.1
+    logits[::2, 1000:1200] = 3.0
+    ids, w = _route(logits, 32)
+    rid, rw = oracle.route(logits.numpy(), 32)
+    assert np.array_equal(ids, rid)
+    assert np.max(np.abs(w - rw)) <= 2e-6
+
+
 def test_router_neg_inf_and_empty():
     logits = torch.randn(64, 112)
     logits[:, :50] = float("-inf")
