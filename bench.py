@@ -444,12 +444,86 @@ def run_ours(args, world, rank, local, pg):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.tokens, args.cpu_sample)
-    if args.prefill and args.config == "tp8_decode":
+    tables = [t for t in args.tables.split(",") if t] if args.config == "tp8_decode" else []
+    if tables:
         del ctx, w13, w13s, w2, w2s
         torch.cuda.empty_cache()
+    if "router" in tables:
+        result["router"] = router_row(device, flush, pg, world)
+    if "ep" in tables:
+        result["ep_emulation"] = ep_rows(device, flush, pg, world)
+        select_config(args.config)
+    if "prefill" in tables:
         result["prefill"] = prefill_table(device, flush, pg, world)
         select_config(args.config)
     return result
+
+
+ROUTER_SHAPE = (32768, 896, 16)  # tokens, router logits per token (experts), top-k
+
+
+def router_row(device, flush, pg, world, steps=10, warmup=3):
+    """The top-k softmax router on a prefill-sized batch: us/call and its fraction of
+    HBM (logits read once, ids and weights written once), L2 flushed before every call."""
+    import quantized_moe_expert_sort_gb300 as moe
+    T, Er, Kr = ROUTER_SHAPE
+    logits = inputs.make_router_logits(T, Er, SEED).to(device)
+    ms = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        moe.route(logits, Kr)
+        e.record()
+        torch.cuda.synchronize(device)
+        if i >= warmup:
+            ms.append(s.elapsed_time(e))
+    us = max_over_ranks(pg, statistics.mean(ms), device) * 1000.0 / world
+    nbytes = T * Er * 4 + T * Kr * 8
+    peak, _ = measured_peaks()
+    log("router T=%d E=%d K=%d: %.1f us" % (T, Er, Kr, us))
+    return {"tokens": T, "experts": Er, "topk": Kr, "us_per_call": round(us, 1), "bound": "hbm",
+            "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+
+
+EP_RANKS, EP_LOCAL_EXPERTS, EP_TOKENS = 8, 112, (128, 1024)
+
+
+def ep_rows(device, flush, pg, world, steps=5, warmup=3):
+    """Expert-parallel forward of the wide shape (8 ranks x 112 experts, inter 3072, a8 SiTUv2)
+    emulated on this GPU: us/call and the whole-call HBM fraction (the active experts'
+    weights of all ranks, x, the intermediate, out and the fp8 combine wire)."""
+    import quantized_moe_expert_sort_gb300 as moe
+    global E
+    select_config("ep_wide")
+    E = EP_RANKS * EP_LOCAL_EXPERTS
+    w13, w13s, w2, w2s = device_weights(device)
+    ep = moe.MoEEP(H, I, EP_LOCAL_EXPERTS, EP_RANKS, K, max(EP_TOKENS), device=device.index or 0)
+    rows = {}
+    peak, _ = measured_peaks()
+    for T in EP_TOKENS:
+        x = inputs.make_x(T, H, SEED).to(device)
+        ids, w = inputs.make_routing(T, E, K, "uniform", SEED)
+        ids, w = ids.to(device), w.to(device)
+        ms = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            ep.forward(x, ids, w, w13, w13s, w2, w2s, "situv2", 4.0, 25.0, "fp8")
+            e.record()
+            torch.cuda.synchronize(device)
+            if i >= warmup:
+                ms.append(s.elapsed_time(e))
+        us = max_over_ranks(pg, statistics.mean(ms), device) * 1000.0 / world
+        n_active = int(torch.unique(ids).numel())
+        ab = algo_bytes(T, n_active, T * K)["call"] + EP_RANKS * T * H * (1 + 1 / 32)  # + the fp8 wire
+        rows["T%d" % T] = {"us_per_call": round(us, 1), "bound": "hbm", "call_frac": round(ab / (peak * 1e9) / (us * 1e-6), 4),
+                           "active_experts": n_active, "ranks": EP_RANKS}
+        log("EP emulation T=%d: %.1f us" % (T, us))
+    del ep, w13, w13s, w2, w2s
+    torch.cuda.empty_cache()
+    return rows
 
 
 PREFILL_ROWS = [("tp8_a8", 4096, "situv2"), ("ep_wide", 8192, "situv2"), ("tp8_a4_zipf", 32768, "situv2")]
@@ -571,7 +645,9 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prepack", action="store_true", help="stage 2 reads a prepacked copy of w2 (moe_prepack)")
-    ap.add_argument("--prefill", type=int, default=1, help="add the prefill table (default workload only)")
+    ap.add_argument("--tables", default="router,ep,prefill",
+                    help="extra rows of the default workload's line: router, ep (expert-parallel emulation), "
+                         "prefill; empty for none")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

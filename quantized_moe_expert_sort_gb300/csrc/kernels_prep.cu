@@ -386,6 +386,19 @@ __device__ __forceinline__ void scatter_units(const __nv_bfloat16* __restrict__ 
         }
       }
     }
+    // Scale bytes of blocks 4i..4i+3 of the warp's token packed into one word (quads
+    // 0 and 4 of the warp hold the words): when H / 32 % 8 == 0 a warp's 8 units are
+    // blocks 8j..8j+7 of one token, and the 4 bytes are adjacent in both scale layouts.
+    const bool pack = nb % 8 == 0;
+    uint32_t sw[kTerms];
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt) {
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc[tt], 4);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc[tt], 8);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc[tt], 12);
+      sw[tt] = sc[tt] | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+    const bool sw_lane = ((lane >> 2) & 3) == 0;  // quads 0 and 4: blocks b .. b + 3, b % 4 == 0
     // the whole block's codes in every thread of the quad
     uint32_t full[kTerms][4 * kWords];
 #pragma unroll
@@ -415,11 +428,16 @@ __device__ __forceinline__ void scatter_units(const __nv_bfloat16* __restrict__ 
       }
       if (CHUNK) {  // tcgen05.cp chunks of 128-row tiles (many-rows path)
         const int m = r & 127;
-        so.scales[((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (m & 31) + 4 * (m >> 5) + (b & 3)] =
-            (uint8_t)sc[0];
+        const size_t o = ((size_t)(r >> 7) * (nb / 4) + (b >> 2)) * 512 + 16 * (m & 31) + 4 * (m >> 5);
+        if (!pack) so.scales[o + (b & 3)] = (uint8_t)sc[0];
+        else if (sw_lane) *reinterpret_cast<uint32_t*>(so.scales + o) = sw[0];
       } else {
 #pragma unroll
-        for (int tt = 0; tt < kTerms; ++tt) so.scales[((size_t)r * kTerms + tt) * so.sstride + b] = (uint8_t)sc[tt];
+        for (int tt = 0; tt < kTerms; ++tt) {
+          const size_t o = ((size_t)r * kTerms + tt) * so.sstride + b;
+          if (!pack) so.scales[o] = (uint8_t)sc[tt];
+          else if (sw_lane) *reinterpret_cast<uint32_t*>(so.scales + o) = sw[tt];
+        }
       }
     }
   }
