@@ -24,6 +24,12 @@
 // quantised logit grid), the warp falls back to K rounds of "take the largest
 // remaining": the maximum of the lanes' current best (value, then lowest id)
 // with two hardware reductions, the owner lane marking it and rescanning.
+//
+// Two kernels share these steps. For E <= 1024 (route_reg_kernel) each lane
+// keeps its PER = E/32 (rounded up to 4, 8, 16 or 32) logits in registers as
+// order keys, read with 16-byte loads when E % 4 == 0: no shared-memory staging,
+// and the per-lane passes unroll. Larger E (up to 4096) stages the row in
+// shared memory (route_topk_kernel).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -49,6 +55,153 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Candidate list (rank step) and chosen slots of one warp, in shared memory.
+struct RouteCand {
+  uint32_t ckey[kCandMax];
+  int32_t cid[kCandMax];
+  uint32_t skey[ROUTE_MAX_TOPK];
+  int32_t sid[ROUTE_MAX_TOPK];
+};
+
+// Register-resident router for E <= 32 * PER. Lane l holds the logits of
+// elements eid(j), j < PER: with VEC (E % 4 == 0, 16-byte aligned rows) the 4
+// floats of 16-byte word l + 32 (j / 4), else element l + 32 j. Slots past E
+// hold -inf and are excluded by their index. Logits are compared as floats
+// (-0 == +0, as in the order-key kernel; NaN is outside the contract), ties by id.
+//
+// The K-th largest lane maximum comes from a bitonic sort of the 32 maxima
+// across the warp; up to 32 candidates are put in (logit desc, id asc) order by
+// a second bitonic sort, so lane k holds the k-th expert.
+template <int PER, bool VEC>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_reg_kernel(const float* __restrict__ logits, int T, int E,
+                                                                     int K, int32_t* __restrict__ ids,
+                                                                     float* __restrict__ weights) {
+  __shared__ RouteCand cand[kRouteWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  RouteCand* rc = cand + warp;
+  const float ninf = -__int_as_float(0x7F800000);
+  auto eid = [&](int j) { return VEC ? 4 * (lane + 32 * (j >> 2)) + (j & 3) : lane + 32 * j; };
+  for (long t = (long)blockIdx.x * kRouteWarps + warp; t < T; t += (long)gridDim.x * kRouteWarps) {
+    const float* src = logits + t * E;
+    float v[PER];
+    if (VEC) {
+#pragma unroll
+      for (int j4 = 0; j4 < PER / 4; ++j4) {
+        const int q = lane + 32 * j4;
+        float4 w = make_float4(ninf, ninf, ninf, ninf);
+        if (4 * q < E) w = __ldg(reinterpret_cast<const float4*>(src) + q);
+        v[4 * j4] = w.x;
+        v[4 * j4 + 1] = w.y;
+        v[4 * j4 + 2] = w.z;
+        v[4 * j4 + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? __ldg(src + e) : ninf;
+      }
+    }
+    // 1. threshold: the K-th largest lane maximum (bitonic sort, descending)
+    float s = ninf;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) s = fmaxf(s, v[j]);
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, s, j);
+        s = (((lane & j) == 0) == ((lane & k) == 0)) ? fmaxf(s, o) : fminf(s, o);
+      }
+    const float t0 = __shfl_sync(0xFFFFFFFFu, s, K - 1);
+    // candidates: this lane's count, an exclusive prefix over the lanes
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) cnt += (v[j] >= t0 && eid(j) < E) ? 1 : 0;
+    int pre = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xFFFFFFFFu, pre, o);
+      if (lane >= o) pre += x;
+    }
+    const int C = __shfl_sync(0xFFFFFFFFu, pre, 31);
+    float my_v = ninf;
+    int my_id = 0;
+    if (C <= kCandMax) {
+      int pos = pre - cnt;
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (v[j] >= t0 && eid(j) < E) {
+          rc->ckey[pos] = __float_as_uint(v[j]);
+          rc->cid[pos] = eid(j);
+          ++pos;
+        }
+      __syncwarp();
+      if (C <= 32) {
+        // 2. bitonic sort of the candidates by (logit desc, id asc); padding lanes sort last
+        float ck = lane < C ? __uint_as_float(rc->ckey[lane]) : ninf;
+        int ci = lane < C ? rc->cid[lane] : 0x7FFFFFFF;
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+          for (int j = k >> 1; j > 0; j >>= 1) {
+            const float ok = __shfl_xor_sync(0xFFFFFFFFu, ck, j);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, ci, j);
+            const bool o_first = ok > ck || (ok == ck && oi < ci);  // the partner comes first
+            const bool keep_first = ((lane & j) == 0) == ((lane & k) == 0);
+            if (keep_first ? o_first : !o_first) { ck = ok; ci = oi; }
+          }
+        my_v = ck;
+        my_id = ci;
+      } else {
+        // 2. rank the candidates; slot < K is the output position
+        for (int c = lane; c < C; c += 32) {
+          const float k = __uint_as_float(rc->ckey[c]);
+          const int id = rc->cid[c];
+          int r = 0;
+          for (int d = 0; d < C; ++d) {
+            const float kd = __uint_as_float(rc->ckey[d]);
+            r += (kd > k) || (kd == k && rc->cid[d] < id);
+          }
+          if (r < K) { rc->skey[r] = __float_as_uint(k); rc->sid[r] = id; }
+        }
+        __syncwarp();
+        if (lane < K) { my_v = __uint_as_float(rc->skey[lane]); my_id = rc->sid[lane]; }
+      }
+      __syncwarp();
+    } else {
+      // K rounds of "take the largest remaining" (bit j of taken: slot j chosen)
+      uint32_t taken = 0u;
+      for (int k = 0; k < K; ++k) {
+        uint32_t bk = 0u;  // order key of the best live slot (0: none)
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int e = eid(j);
+          const uint32_t kj = order_key(v[j]);
+          if (e < E && !((taken >> j) & 1u) && (kj > bk || (kj == bk && e < bi))) { bk = kj; bi = e; }
+        }
+        const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == kmax ? (uint32_t)bi : 0x7FFFFFFFu);
+        if (lane == k) { my_v = key_value(kmax); my_id = win; }
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+          if (eid(j) == win) taken |= 1u << j;
+      }
+    }
+    const float lmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+    float ex = 0.0f;
+    if (lane < K) ex = expf(my_v - lmax);
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane < K) {
+      ids[t * K + lane] = my_id;
+      weights[t * K + lane] = ex / sum;
+    }
+  }
 }
 
 }  // namespace
@@ -170,7 +323,21 @@ cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids,
   const long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  route_topk_kernel<<<(unsigned)blocks, kRouteWarps * 32, route_smem_bytes(E), st>>>(logits, T, E, K, ids, weights);
+  const dim3 g((unsigned)blocks), b(kRouteWarps * 32);
+  const bool vec = E % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  if (E <= 1024) {
+    // PER: the smallest of 4, 8, 16, 32 with 32 * PER >= E
+#define MOE_ROUTE_REG(P)                                                                               \
+  (vec ? route_reg_kernel<P, true><<<g, b, 0, st>>>(logits, T, E, K, ids, weights)                      \
+       : route_reg_kernel<P, false><<<g, b, 0, st>>>(logits, T, E, K, ids, weights))
+    if (E <= 128) MOE_ROUTE_REG(4);
+    else if (E <= 256) MOE_ROUTE_REG(8);
+    else if (E <= 512) MOE_ROUTE_REG(16);
+    else MOE_ROUTE_REG(32);
+#undef MOE_ROUTE_REG
+  } else {
+    route_topk_kernel<<<g, b, route_smem_bytes(E), st>>>(logits, T, E, K, ids, weights);
+  }
   return cudaGetLastError();
 }
 

@@ -42,6 +42,19 @@ def test_router_ids_bit_exact(T, E, K, grid):
     assert np.max(np.abs(w - rw)) <= 2e-6
 
 
+@pytest.mark.parametrize("E,K", [(200, 8), (255, 16), (500, 32), (512, 4), (1000, 16), (1023, 32), (1024, 1)])
+def test_router_every_register_width(E, K):
+    # E <= 1024 runs the register-resident kernel (4, 8, 16 or 32 logits per lane;
+    # 16-byte loads when E % 4 == 0); half the rows carry a coarse grid of ties
+    g = torch.Generator().manual_seed(E * 31 + K)
+    logits = torch.randn(300, E, generator=g)
+    logits[1::2] = torch.round(logits[1::2] * 2) / 2
+    ids, w = _route(logits, K)
+    rid, rw = oracle.route(logits.numpy(), K)
+    assert np.array_equal(ids, rid)
+    assert np.max(np.abs(w - rw)) <= 2e-6
+
+
 def test_router_all_equal_and_candidate_overflow():
     # all logits equal: every element passes the lane-maximum threshold, so the
     # exact fallback selection runs; ids are 0..K-1, weights 1/K
