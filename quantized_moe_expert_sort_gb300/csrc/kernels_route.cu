@@ -20,8 +20,9 @@
 //     K = 16) there are about 30 of them.
 //  2. Rank. Each candidate's output slot is the number of candidates before it
 //     in (logit descending, id ascending) order; slots below K are the result.
-// When more than kCandMax elements pass the threshold (heavy ties, e.g. a
-// quantised logit grid), the warp falls back to K rounds of "take the largest
+// When more candidates pass the threshold than the rank step takes (128 in the
+// register kernel, 512 in the shared-memory one: heavy ties, e.g. a quantised
+// logit grid), the warp falls back to K rounds of "take the largest
 // remaining": the maximum of the lanes' current best (value, then lowest id)
 // with two hardware reductions, the owner lane marking it and rescanning.
 //
@@ -37,11 +38,12 @@ namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
-constexpr int kCandMax = 128;  // candidates above the threshold the rank step takes
+constexpr int kCandMax = 128;      // candidates above the threshold the rank step takes (E <= 1024)
+constexpr int kCandMaxWide = 512;  // the same for the shared-memory kernel (E up to 4096)
 
 struct RouteScratch {  // per warp, after the staged logits rows
-  uint32_t ckey[kCandMax];
-  int32_t cid[kCandMax];
+  uint32_t ckey[kCandMaxWide];
+  int32_t cid[kCandMaxWide];
   uint32_t skey[ROUTE_MAX_TOPK];
   int32_t sid[ROUTE_MAX_TOPK];
 };
@@ -246,13 +248,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const floa
       const bool pass = e < E && k >= t0;
       const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
       const int pos = C + __popc(b & lt_mask);
-      if (pass && pos < kCandMax) { rs->ckey[pos] = k; rs->cid[pos] = e; }
+      if (pass && pos < kCandMaxWide) { rs->ckey[pos] = k; rs->cid[pos] = e; }
       C += __popc(b);
     }
     __syncwarp();
     uint32_t my_key = 0u;
     int my_id = 0;
-    if (C <= kCandMax) {
+    if (C <= kCandMaxWide) {
       // 2. rank the candidates; slot < K is the output position
       for (int c = lane; c < C; c += 32) {
         const uint32_t k = rs->ckey[c];
@@ -317,26 +319,42 @@ cudaError_t route_set_smem_limits() {
                               (int)route_smem_bytes(ROUTE_MAX_EXPERTS));
 }
 
+// Grid of one wave: CTAs resident at once (the kernel's occupancy, looked up once),
+// tokens spread so that every warp takes ceil(T / warps) of them.
+template <int P, bool V> static unsigned route_grid(int T, int num_sms) {
+  static int occ = 0;  // per instantiation
+  if (occ == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, route_reg_kernel<P, V>, kRouteWarps * 32, 0) != cudaSuccess)
+    occ = 1;
+  const long resident = (long)(occ > 0 ? occ : 1) * num_sms;
+  const long per_warp = ((long)T + resident * kRouteWarps - 1) / (resident * kRouteWarps);
+  const long blocks = ((long)T + per_warp * kRouteWarps - 1) / (per_warp * kRouteWarps);
+  return (unsigned)(blocks > 0 ? blocks : 1);
+}
+
 cudaError_t launch_route(const float* logits, int T, int E, int K, int32_t* ids, float* weights, int num_sms,
                          cudaStream_t st) {
   long blocks = ((long)T + kRouteWarps - 1) / kRouteWarps;
   const long cap = (long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const dim3 g((unsigned)blocks), b(kRouteWarps * 32);
+  const dim3 b(kRouteWarps * 32);
   const bool vec = E % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
   if (E <= 1024) {
-    // PER: the smallest of 4, 8, 16, 32 with 32 * PER >= E
-#define MOE_ROUTE_REG(P)                                                                               \
-  (vec ? route_reg_kernel<P, true><<<g, b, 0, st>>>(logits, T, E, K, ids, weights)                      \
-       : route_reg_kernel<P, false><<<g, b, 0, st>>>(logits, T, E, K, ids, weights))
+    // PER: the smallest of 4, 8, 16, 32 with 32 * PER >= E. One wave of resident
+    // CTAs, each warp taking the same number of tokens (no partial last wave).
+#define MOE_ROUTE_REG(P)                                                                                   \
+  (vec ? route_reg_kernel<P, true><<<route_grid<P, true>(T, num_sms), b, 0, st>>>(       \
+             logits, T, E, K, ids, weights)                                                                 \
+       : route_reg_kernel<P, false><<<route_grid<P, false>(T, num_sms), b, 0, st>>>(     \
+             logits, T, E, K, ids, weights))
     if (E <= 128) MOE_ROUTE_REG(4);
     else if (E <= 256) MOE_ROUTE_REG(8);
     else if (E <= 512) MOE_ROUTE_REG(16);
     else MOE_ROUTE_REG(32);
 #undef MOE_ROUTE_REG
   } else {
-    route_topk_kernel<<<g, b, route_smem_bytes(E), st>>>(logits, T, E, K, ids, weights);
+    route_topk_kernel<<<dim3((unsigned)blocks), b, route_smem_bytes(E), st>>>(logits, T, E, K, ids, weights);
   }
   return cudaGetLastError();
 }
