@@ -122,18 +122,40 @@ __device__ __forceinline__ float tanh_act(float z) {
   return 2.0f * fast_sigmoid(2.0f * z) - 1.0f;
 }
 
+// Per-call constants of the activation: -2 log2(e) / beta, -2 log2(e) / lbeta and
+// beta * lbeta (formed once per thread instead of two divisions per value).
+struct ActK {
+  float nb2, nlb2, blb;
+};
+__device__ __forceinline__ ActK act_consts(float beta, float lbeta) {
+  return ActK{-2.0f * 1.4426950408889634f / beta, -2.0f * 1.4426950408889634f / lbeta, beta * lbeta};
+}
+
 // kAccurate: tanh_act (the bf16 intermediate of the a16 path keeps 8 bits of every
-// value); otherwise 2 * sigmoid(2z) - 1 throughout, whose worst relative error
-// (~4e-4 at small z) lies far inside the fp8 / fp4 steps the intermediate is
-// requantised to.
+// value). Otherwise (fp8 / fp4 intermediates) tanh(z) = (1 - e^-2z) / (1 + e^-2z),
+// whose worst relative error (~4e-4 at small z, from the cancellation) lies far
+// inside the fp8 / fp4 steps the intermediate is requantised to, and the three
+// factors of SiTUv2 share one reciprocal:
+//   y = beta * lbeta * (1 - e1)(1 - e3) / ((1 + e1)(1 + e2)(1 + e3)),
+//   e1 = e^(-2g/beta), e2 = e^(-g), e3 = e^(-2u/lbeta),
+// three exp2 and one reciprocal per value. e1 and e3 are capped at 2^40 (tanh is
+// -1 to within 2^-39 there) so that the denominator stays finite; sigmoid(g) for
+// g < -27 is below what that form resolves and takes the per-factor form.
 template <bool kAccurate = true>
-__device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta) {
-  const float sig = fast_sigmoid(g);
-  if (act == ACT_SILU) return g * sig * u;
-  if (kAccurate) return beta * tanh_act(g / beta) * sig * (lbeta * tanh_act(u / lbeta));
-  const float tg = 2.0f * fast_sigmoid(2.0f * g / beta) - 1.0f;
-  const float tu = 2.0f * fast_sigmoid(2.0f * u / lbeta) - 1.0f;
-  return beta * tg * sig * (lbeta * tu);
+__device__ __forceinline__ float act_apply(int act, float g, float u, float beta, float lbeta, const ActK& k) {
+  if (act == ACT_SILU) return g * fast_sigmoid(g) * u;
+  if (kAccurate) return beta * tanh_act(g / beta) * fast_sigmoid(g) * (lbeta * tanh_act(u / lbeta));
+  if (g < -27.0f) {
+    const float tg = 2.0f * fast_sigmoid(2.0f * g / beta) - 1.0f;
+    const float tu = 2.0f * fast_sigmoid(2.0f * u / lbeta) - 1.0f;
+    return beta * tg * fast_sigmoid(g) * (lbeta * tu);
+  }
+  float e1, e2, e3, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fminf(g * k.nb2, 40.0f)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"(-1.4426950408889634f * g));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e3) : "f"(fminf(u * k.nlb2, 40.0f)));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"((1.0f + e1) * (1.0f + e2) * (1.0f + e3)));
+  return k.blb * ((1.0f - e1) * (1.0f - e3)) * r;
 }
 
 // ---------------------------------------------------------------------------

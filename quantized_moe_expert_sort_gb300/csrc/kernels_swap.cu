@@ -765,12 +765,13 @@ __global__ void __launch_bounds__(threads_sw<STAGE>(), 1) swap_stage_kernel(Stag
         const int j = ui.tile * 128 + 32 * q + lane;  // intermediate column of this lane
         // y = act(g, u) of item rows [c0, c0 + 16), requantised per 32 along I across the
         // warp (one out-of-line call per row keeps this rarely repeated code small)
+        const ActK ak = act_consts(p.beta, p.lbeta);
         auto requant_rows = [&](int c0, const float* gv, const float* uv) {
           const int nn = min(16, nrows - c0);
 #pragma unroll
           for (int n = 0; n < 16; ++n)
             if (n < nn)
-              requant_row<KD::kTerms, KD::kMxf4>(act_apply<(KD::kTerms > 1)>(p.act, gv[n], uv[n], p.beta, p.lbeta), row0 + c0 + n, j,
+              requant_row<KD::kTerms, KD::kMxf4>(act_apply<(KD::kTerms > 1)>(p.act, gv[n], uv[n], p.beta, p.lbeta, ak), row0 + c0 + n, j,
                                                  lane, I, p.oq, p.os, p.os_stride);
         };
         bool ok = true;

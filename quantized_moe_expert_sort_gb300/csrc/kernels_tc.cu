@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
     const int grp = (warp - 4) >> 2;       // column group: 0 -> warps 4-7, 1 -> warps 8-11
     const int m = 32 * q + lane;           // tile row of this thread (= TMEM lane)
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const ActK ak = act_consts(p.beta, p.lbeta);
     int lt = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++lt) {
       int b, nt;
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_stage_kernel(TcParams p, con
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            y[i] = act_apply<false>(p.act, __uint_as_float(gr[i]), __uint_as_float(ur[i]), p.beta, p.lbeta);
+            y[i] = act_apply<false>(p.act, __uint_as_float(gr[i]), __uint_as_float(ur[i]), p.beta, p.lbeta, ak);
             amax = fmaxf(amax, fabsf(y[i]));
           }
           if (valid) {
