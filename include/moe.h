@@ -197,9 +197,11 @@ moe_status moe_forward(moe_ctx* ctx, const void* x, const int32_t* topk_ids, con
 
 /* moe_forward with HOST buffers for the per-call data: x_host (bf16 [T,H]),
  * topk_ids_host, topk_weights_host and out_host (bf16 [T,H]) live in host
- * memory (pinned memory makes the copies asynchronous); the weights are device
- * pointers. Copies the inputs into ctx-owned device staging, runs moe_forward,
- * copies the result back and synchronises `stream` before returning. */
+ * memory; the weights are device pointers. A buffer in page-locked memory that
+ * the device can address (cudaHostAlloc / cudaMallocHost memory under unified
+ * addressing, e.g. torch's pin_memory) is read or written by the kernels in
+ * place, over the host link; any other buffer is copied through ctx-owned
+ * device staging. Synchronises `stream` before returning. */
 moe_status moe_forward_host(moe_ctx* ctx, const void* x_host, const int32_t* topk_ids_host,
                             const float* topk_weights_host, int num_tokens, const uint8_t* w13,
                             const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale, int act,

@@ -772,13 +772,40 @@ moe_status moe_forward_host(moe_ctx* c, const void* x_host, const int32_t* ids_h
   CUDA_TRY(cudaSetDevice(c->device));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t xb = (size_t)T * c->H * 2, pb = (size_t)T * c->K;
-  CUDA_TRY(cudaMemcpyAsync(c->st_x, x_host, xb, cudaMemcpyHostToDevice, st));
-  CUDA_TRY(cudaMemcpyAsync(c->st_ids, ids_host, pb * sizeof(int32_t), cudaMemcpyHostToDevice, st));
-  CUDA_TRY(cudaMemcpyAsync(c->st_w, w_host, pb * sizeof(float), cudaMemcpyHostToDevice, st));
-  moe_status s = moe_forward(c, c->st_x, c->st_ids, c->st_w, T, w13, w13s, w2, w2s, act, beta, lbeta, adt,
-                             c->st_out, stream);
-  if (s != MOE_OK) return s;
-  CUDA_TRY(cudaMemcpyAsync(out_host, c->st_out, xb, cudaMemcpyDeviceToHost, st));
+  // Page-locked host memory the device can address is used in place (the kernels
+  // read x, ids and weights and write out across the host link: no copy launches);
+  // anything else goes through the device staging buffers.
+  auto in_place = [&](const void* h) -> void* {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+      cudaGetLastError();  // (clear: an unknown pointer is not an error here)
+      return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+  };
+  const void* x = in_place(x_host);
+  const int32_t* ids = static_cast<const int32_t*>(in_place(ids_host));
+  const float* w = static_cast<const float*>(in_place(w_host));
+  void* out = in_place(out_host);
+  if (!x) {
+    CUDA_TRY(cudaMemcpyAsync(c->st_x, x_host, xb, cudaMemcpyHostToDevice, st));
+    x = c->st_x;
+  }
+  if (!ids) {
+    CUDA_TRY(cudaMemcpyAsync(c->st_ids, ids_host, pb * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    ids = c->st_ids;
+  }
+  if (!w) {
+    CUDA_TRY(cudaMemcpyAsync(c->st_w, w_host, pb * sizeof(float), cudaMemcpyHostToDevice, st));
+    w = c->st_w;
+  }
+  moe_status s = moe_forward(c, x, ids, w, T, w13, w13s, w2, w2s, act, beta, lbeta, adt, out ? out : c->st_out,
+                             stream);
+  if (s != MOE_OK) {
+    cudaStreamSynchronize(st);  // copies already enqueued finish before the caller reuses its buffers
+    return s;
+  }
+  if (!out) CUDA_TRY(cudaMemcpyAsync(out_host, c->st_out, xb, cudaMemcpyDeviceToHost, st));
   CUDA_TRY(cudaStreamSynchronize(st));
   return MOE_OK;
 }

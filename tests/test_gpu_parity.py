@@ -346,6 +346,13 @@ def test_forward_host_matches_device_and_zero_tokens():
     hout = ctx.forward_host(case["x"].pin_memory(), case["ids"].pin_memory(), case["w"].pin_memory(),
                             d["w13"], d["w13s"], d["w2"], d["w2s"], "situv2", 4.0, 25.0, "bf16")
     assert torch.equal(hout, out.cpu()) or token_rel_l2(hout.float().numpy(), out.float().cpu().numpy()) < 1e-3
+    # pinned buffers are used in place, pageable ones go through the staging copies;
+    # every mix gives the same result
+    for pin in ((False, False, False, False), (True, False, True, False), (False, True, False, True)):
+        args = [t.pin_memory() if p else t.clone() for t, p in zip((case["x"], case["ids"], case["w"]), pin[:3])]
+        o = torch.empty((16, 256), dtype=torch.bfloat16, pin_memory=pin[3])
+        ctx.forward_host(*args, d["w13"], d["w13s"], d["w2"], d["w2s"], "situv2", 4.0, 25.0, "bf16", out=o)
+        assert token_rel_l2(o.float().numpy(), out.float().cpu().numpy()) < 1e-3, pin
     empty = ctx.forward(d["x"][:0], d["ids"][:0], d["w"][:0], d["w13"], d["w13s"], d["w2"], d["w2s"])
     assert empty.shape == (0, 256)
 
