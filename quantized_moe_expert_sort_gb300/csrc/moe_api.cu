@@ -590,10 +590,20 @@ static moe_status forward_impl(moe_ctx* c, const void* x, const int32_t* ids, co
       if (!c->split_cap[swkind][k]) c->split_cap[swkind][k] = 1 + swap_split_max_clusters(swkind, k);
       return (long)c->split_cap[swkind][k] - 1;
     };
+    // Also split in two when the units, taken in turn by persistent clusters of two
+    // (each unit half as long), end in fewer rounds than on single CTAs: units just
+    // above one SM each (T = 4: 186 units on 152 SMs take two rounds, on ~70 pairs
+    // three half-length ones). Measured faster for bf16 and fp8 activations (TP8,
+    // T = 4: 66.9 -> 63.6 and 76.8 -> 72.6 us) and slower for fp4 (50.2 -> 54.3 us),
+    // whose items are shorter.
     int ks = 1;
     if (c->split_k && kt1 >= 3 && u1 <= cap(3)) ks = 3;
     else if (c->split_k && kt1 >= 2 && u1 <= cap(2)) ks = 2;
-    const long g1 = ks > 1 ? u1 * ks : (u1 < c->num_sms ? u1 : c->num_sms);
+    else if (c->split_k && swkind != SW_A4 && kt1 >= 2 && cap(2) > 0) {
+      const long r1 = (u1 + c->num_sms - 1) / c->num_sms, r2 = (u1 + cap(2) - 1) / cap(2);
+      if (r2 < 2 * r1) ks = 2;
+    }
+    const long g1 = ks > 1 ? (u1 < cap(ks) ? u1 : cap(ks)) * ks : (u1 < c->num_sms ? u1 : c->num_sms);
     e = launch_swap_stage(swkind, 1, false, ks, q1, c->tm_w13sw, tm_xs, (int)g1, st);
     if (e != cudaSuccess) return cuda_fail(e, "stage-1 launch");
     StageParams q2 = p2;
