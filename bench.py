@@ -440,7 +440,9 @@ def run_ours(args, world, rank, local, pg):
         "clocks": clocks,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call",
                 "h2d_bytes_per_step": args.tokens * H * 2 + args.tokens * K * 8,
-                "d2h_bytes_per_step": args.tokens * H * 2},
+                "d2h_bytes_per_step": args.tokens * H * 2,
+                "transfer": "moe_forward_host on pinned host tensors: the kernels read x, ids and weights "
+                            "and write out across the host link (no staging copies)"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.tokens, args.cpu_sample)
