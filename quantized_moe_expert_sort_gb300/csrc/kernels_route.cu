@@ -11,26 +11,27 @@
 // the chosen K alone (the full-softmax denominator cancels):
 //   w_k = exp(l_k - l_max) / sum_j exp(l_j - l_max),  j over the K chosen.
 //
-// One warp per token; the logits row is staged in shared memory, lane l owning
-// elements l, l + 32, ....  Selection is exact in two steps:
+// One warp per token. Selection is exact in two steps:
 //  1. Threshold. With t0 the K-th largest of the 32 lanes' maxima, at least K
 //     elements are >= t0 (those K maxima), so the K-th largest logit is >= t0
 //     and every element of the top K -- ties at the boundary included -- is
 //     among the candidates {e : l_e >= t0}.  For Gaussian logits (E = 896,
 //     K = 16) there are about 30 of them.
-//  2. Rank. Each candidate's output slot is the number of candidates before it
-//     in (logit descending, id ascending) order; slots below K are the result.
-// When more candidates pass the threshold than the rank step takes (128 in the
+//  2. Order. The candidates are put in (logit descending, id ascending) order;
+//     the first K are the result.
+// When more candidates pass the threshold than step 2 takes (128 in the
 // register kernel, 512 in the shared-memory one: heavy ties, e.g. a quantised
 // logit grid), the warp falls back to K rounds of "take the largest
 // remaining": the maximum of the lanes' current best (value, then lowest id)
-// with two hardware reductions, the owner lane marking it and rescanning.
+// with two hardware reductions, the owner lane marking it.
 //
-// Two kernels share these steps. For E <= 1024 (route_reg_kernel) each lane
-// keeps its PER = E/32 (rounded up to 4, 8, 16 or 32) logits in registers as
-// order keys, read with 16-byte loads when E % 4 == 0: no shared-memory staging,
-// and the per-lane passes unroll. Larger E (up to 4096) stages the row in
-// shared memory (route_topk_kernel).
+// Two kernels. For E <= 1024 (route_reg_kernel) each lane keeps its PER = E/32
+// (rounded up to 4, 8, 16 or 32) logits in registers, read with 16-byte loads
+// when E % 4 == 0; t0 comes from a bitonic sort of the 32 lane maxima across
+// the warp, and up to 32 candidates are ordered by a second bitonic sort (more:
+// each candidate's slot is the number of candidates before it). Larger E (up to
+// 4096, route_topk_kernel) stages the row in shared memory, lane l owning
+// elements l, l + 32, ..., and ranks the candidates.
 #include "common.cuh"
 #include "kernels.h"
 
