@@ -241,6 +241,24 @@ def tensor_peak_tflops(a_dtype):
     return 1900.0 * TENSOR_RATIO[a_dtype], "fallback bf16 burst x nominal kind ratio"
 
 
+def kernel_roofline(nbytes, nflops, t_ms, peak_gbs, peak_src, tpeak_tflops, tpeak_src):
+    """A kernel against its governing bound: the slower of its algorithmic bytes at the
+    HBM peak and its algorithmic FLOPs at the tensor peak of its MMA kind."""
+    t = t_ms * 1e-3
+    if nflops / (tpeak_tflops * 1e12) > nbytes / (peak_gbs * 1e9):
+        achieved, kpeak, unit, src, bound = nflops / t / 1e12, tpeak_tflops, "TFLOP/s", tpeak_src, "tensor"
+    else:
+        achieved, kpeak, unit, src, bound = nbytes / t / 1e9, peak_gbs, "GB/s", peak_src, "hbm"
+    return {"bound": bound, "achieved": round(achieved, 1), "peak": round(kpeak, 1), "peak_source": src,
+            "unit": unit, "frac": round(achieved / kpeak, 4)}
+
+
+def call_roofline(nbytes, nflops, t_ms, peak_gbs, tpeak_tflops):
+    """(governing bound, fraction) of a whole call: its roofline time over its measured time."""
+    t_bytes, t_flops = nbytes / (peak_gbs * 1e9), nflops / (tpeak_tflops * 1e12)
+    return ("tensor" if t_flops > t_bytes else "hbm"), round(max(t_bytes, t_flops) / (t_ms * 1e-3), 4)
+
+
 def stored_traffic(config, kernel_name, T):
     """DRAM bytes per launch from a committed ncu summary, if it is current."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -367,14 +385,8 @@ def run_ours(args, world, rank, local, pg):
     kflops = {"stage1": 4.0 * n_pairs * H * I, "stage2": 2.0 * n_pairs * H * I, "call": flops}
     # the governing bound of a kernel: the slower of its bytes at the HBM peak and its
     # FLOPs at the tensor peak of the MMA kind it runs
-    t_kernel = per_avg[dominant] * 1e-3
-    tensor_bound = kflops[dominant] / (tpeak * 1e12) > ab[dominant] / (peak * 1e9)
-    if tensor_bound:
-        achieved, kpeak, kunit, ksrc = kflops[dominant] / t_kernel / 1e12, tpeak, "TFLOP/s", tpeak_kind
-    else:
-        achieved, kpeak, kunit, ksrc = ab[dominant] / t_kernel / 1e9, peak, "GB/s", peak_kind
-    t_roof_call = max(ab["call"] / (peak * 1e9), flops / (tpeak * 1e12))
-    call_bound = "tensor" if flops / (tpeak * 1e12) > ab["call"] / (peak * 1e9) else "hbm"
+    roof = kernel_roofline(ab[dominant], kflops[dominant], per_avg[dominant], peak, peak_kind, tpeak, tpeak_kind)
+    call_bound, call_frac = call_roofline(ab["call"], flops, step_ms, peak, tpeak)
     traffic = stored_traffic(args.config, dominant, args.tokens)
 
     # --- sweep over the decode token tiers
@@ -426,14 +438,9 @@ def run_ours(args, world, rank, local, pg):
                    "active_experts": n_active, "routed_pairs": n_pairs,
                    "w2_prepacked": bool(args.prepack),
                    "sweep_us_per_call": sweep, "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "kernel": dominant,
-                     "achieved": round(achieved, 1), "peak": round(kpeak, 1), "peak_source": ksrc, "unit": kunit,
-                     "frac": round(achieved / kpeak, 4),
-                     "traffic": traffic, "algo_bytes_per_launch": ab[dominant],
-                     "algo_flops_per_launch": kflops[dominant],
-                     "call_bound": call_bound,
-                     "call_frac": round(t_roof_call / (step_ms * 1e-3), 4),
-                     "kernel_ms": {k: round(v, 5) for k, v in per_avg.items()}},
+        "roofline": dict(roof, kernel=dominant, traffic=traffic, algo_bytes_per_launch=ab[dominant],
+                         algo_flops_per_launch=kflops[dominant], call_bound=call_bound, call_frac=call_frac,
+                         kernel_ms={k: round(v, 5) for k, v in per_avg.items()}),
         # launches per call, from the launch groups the library recorded (the
         # stand-alone sort is three kernels above 8192 pairs), times the timed calls
         "gpu_launches": sum(3 if name == "sort" and args.tokens * K > 8192 else 1 for name in per_avg) * args.steps,
